@@ -1,0 +1,393 @@
+"""Benchmark of the fused single-pass mHC step (n = 4 streams, d = 5120) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: the projection weights are split into
+their three bf16 planes (mhc_pack_weights) and the fused kernel (mhc_fused_step_packed) reads
+X and F once and writes X', y, p, u, C. The workload is the prefill batch B=4, T=8192
+(N = 32,768 tokens, 3.4 GB of streams per step, far larger than L2), seeded synthetic inputs.
+
+Tokens are independent, so N GPUs run N independent batches (weak scaling, no collective on the
+data path); the printed value is all ranks' tokens over the slowest rank's time.
+
+--impl reference times the CPU oracle (the only reference this method has) on a bounded sample
+of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused mHC step tokens/s at n=4,d=5120; % of HBM roofline (1×GB300)"
+WORKLOAD = "prefill32k"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0}
+STREAM_BYTES_PER_TOKEN = (2 * 4 + 2) * 5120 * 2      # (2n+2) d bf16: read X, F; write X', y
+SMALL_BYTES_PER_TOKEN = 16 + 16 + 64 + 16 + 16 + 64  # p,u,C previous in; p,u,C out (fp32)
+
+
+def algorithmic_bytes(N: int, d: int = 5120) -> int:
+    """Bytes one fused launch must move: the streams and small per-token vectors, plus the packed
+    weights and the gain once."""
+    return N * (STREAM_BYTES_PER_TOKEN + SMALL_BYTES_PER_TOKEN) + 72 * 4 * d * 2 + d * 4
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh), "measured"
+    except Exception:
+        return PEAKS_FALLBACK, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("fused.cu", "ptx.cuh", "mix_math.cuh"):
+        with open(os.path.join(ROOT, "stream_residual_fusion_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(N: int):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, scaled to N
+    tokens; None when the summary was taken on different kernel source."""
+    path = os.path.join(ROOT, "profiles", "fused_step_prefill_ncu.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel source hash:\s*`?([0-9a-f]{16})", text)
+    m_bpt = re.search(r"dram bytes per token:\s*([0-9.]+)", text)
+    if not m_hash or not m_bpt or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bpt.group(1)) * N
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        inside = [r for t, r in self.rows if self.t_on is not None and self.t_on <= t <= self.t_off]
+        rows = inside or [r for _, r in self.rows][-3:]
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "in_timed_region": bool(inside)}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle leg (reported baseline; also the reference arm)
+
+
+def _oracle_chunk(args):
+    seed, lo, hi = args
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import oracle as O
+    from stream_residual_fusion_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    inp = synth.make_inputs(hi - lo, 4, w.d, seed=seed, scale_uniform=w.scale_uniform)
+    a = O.inputs_to_f64(inp)
+    t0 = time.perf_counter()
+    O.fused_step(a["X"], a["F"], a["pre"], a["post"], a["comb"], a["W"], a["scale"], a["base"],
+                 a["gain"])
+    return hi - lo, time.perf_counter() - t0
+
+
+def oracle_throughput(tokens_per_worker: int = 96):
+    """The oracle, as it stands, on a bounded sample of the workload: one spawned single-threaded
+    process per host core, each on its own slice of tokens. Returns (tokens/s, cores, sample)."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    env_keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        jobs = [(7000 + i, 0, tokens_per_worker) for i in range(cores)]
+        t0 = time.perf_counter()
+        with ctx.Pool(cores) as pool:
+            res = pool.map(_oracle_chunk, jobs)
+        wall = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    toks = sum(r[0] for r in res)
+    busy = max(r[1] for r in res)
+    sample = (f"{toks} tokens of the B=4,T=8192 recipe (n=4, d=5120), {cores} spawned "
+              f"single-threaded processes x {tokens_per_worker} tokens; slowest worker {busy:.1f} s "
+              f"(wall {wall:.1f} s incl. start-up)")
+    return toks / busy, cores, sample
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per = max(8, int(os.environ.get("MHC_REF_TOKENS_PER_WORKER", "24")))
+    values = []
+    sample = cores = None
+    for _ in range(args.warmup):
+        oracle_throughput(tokens_per_worker=8)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, cores, sample = oracle_throughput(tokens_per_worker=per)
+        values.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.median(values)
+    from stream_residual_fusion_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wall / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + " (N=32768), n=4, d=5120", "B": w.B, "T": w.T, "n": 4,
+                   "d": w.d, "sample": "bounded per step: see cpu_baseline.sample"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------
+# the GPU arm
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from stream_residual_fusion_gb300 import mhc, synth
+    w = synth.WORKLOADS[WORKLOAD]
+    N, d = w.N, w.d
+    inp = synth.make_workload(w, seed=3000 + rank, device=dev)
+    torch.cuda.synchronize()
+
+    out = {"Xp": torch.empty_like(inp["X"]), "y": torch.empty(N, d, dtype=torch.bfloat16, device=dev),
+           "pre": torch.empty(N, 4, device=dev), "post": torch.empty(N, 4, device=dev),
+           "comb": torch.empty(N, 4, 4, device=dev)}
+    Wp = torch.empty(3 * 24, 4 * d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev_a=None, ev_b=None):
+        mhc.pack_weights(inp["W"], out=Wp, stream=stream)                    # launch 1
+        if ev_a is not None:
+            ev_a.record(stream)
+        mhc.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None,
+                       inp["scale"], inp["base"], inp["gain"], W_packed=Wp, out=out,
+                       stream=stream)                                        # launch 2
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if mhc.get_status() != mhc.MHC_OK:
+        raise RuntimeError("device-side wait gave up during warm-up")
+
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    clocks = ClockSampler(visible[local].strip() if local < len(visible) else local)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_on()
+    t_start.record(stream)
+    for i in range(K):
+        step(*ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_off()
+    if world > 1:
+        dist.barrier()
+    clocks.stop()
+    status = mhc.get_status()
+    total_ms = t_start.elapsed_time(t_end)
+    fused_ms = [a.elapsed_time(b) for a, b in ev]
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = world * N / (ms_per_step / 1e3)
+
+    # ------------------------------------------------------------------ end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(2, min(5, K))
+        host = {k: inp[k].to("cpu").pin_memory() for k in ("X", "F", "pre", "post", "comb")}
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+        dev_in = {k: torch.empty_like(inp[k]) for k in host}
+
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            mhc.pack_weights(inp["W"], out=Wp, stream=stream)
+            mhc.fused_step(dev_in["X"], dev_in["F"], dev_in["pre"], dev_in["post"], dev_in["comb"],
+                           None, inp["scale"], inp["base"], inp["gain"], W_packed=Wp, out=out,
+                           stream=stream)
+            for k, v in out.items():
+                host_out[k].copy_(v, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        te = torch.tensor([a.elapsed_time(b) / e2e_steps], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * N / (float(te.item()) / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": float(te.item()), "steps": e2e_steps}
+        del host, host_out, dev_in
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_kind = measured_peaks()
+    fused_avg = statistics.mean(fused_ms)
+    achieved = algorithmic_bytes(N, d) / (fused_avg / 1e3) / 1e9
+    peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    traffic = ncu_traffic(N)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} (N={N}), n=4, d={d}", "B": w.B, "T": w.T, "n": 4, "d": d,
+                   "sinkhorn_iters": 20, "comb_reading": "code: X'_k = u_k F + sum_j C_jk X_j",
+                   "l2": "inputs larger than L2 (3.4 GB of streams per step)",
+                   "step": "mhc_pack_weights + mhc_fused_step_packed"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "step_kernel<true> (fused)",
+                     "kernel_ms_avg": fused_avg, "kernel_ms_p50": statistics.median(fused_ms),
+                     "kernel_ms_p95": sorted(fused_ms)[int(0.95 * (len(fused_ms) - 1))],
+                     "kernel_ms_p99": sorted(fused_ms)[int(0.99 * (len(fused_ms) - 1))],
+                     "algorithmic_bytes_per_launch": algorithmic_bytes(N, d)},
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "status": "ok" if status == mhc.MHC_OK else "device wait gave up",
+        "gpu": torch.cuda.get_device_name(dev),
+        "torch": torch.__version__,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = oracle_throughput()
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

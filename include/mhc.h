@@ -1,0 +1,161 @@
+/*
+ * mhc.h -- C ABI of libmhc.so, the GB300 (sm_103a) single-pass mHC step.
+ *
+ * The multi-stream hyper-connection (mHC) residual step of a 4-stream block, as defined on the
+ * pages "DeepSeek V4.1 · Stream weights for the feed-forward" (sections "Why", "All 5 steps",
+ * "Parameters", "Code") and "DeepSeek V4.1 · MoE RMSNorm" (formula block, "Code").
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous, row-major, with
+ *     the token axis flattened (N = B*T). bf16 tensors are passed as void*. The library never
+ *     frees or keeps them.
+ *   - Every pointer must be 16-byte aligned (MHC_ERR_ALIGN otherwise).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream). The library never synchronises, except in mhc_get_status.
+ *   - The library allocates no device memory. Calls that need scratch take a caller-owned
+ *     `workspace` of at least the size the matching *_workspace_bytes() call returns.
+ *   - Arguments are validated on the host before anything is launched; a negative return code
+ *     means nothing was launched (except MHC_ERR_CUDA, which reports a launch failure).
+ *   - Only n = 4 streams is built (the shape of the pages' block; (2+n)n = 24 mix numbers).
+ */
+#ifndef MHC_H
+#define MHC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------------ */
+#define MHC_OK             0
+#define MHC_ERR_NULL      -1  /* a required pointer is NULL                                     */
+#define MHC_ERR_SHAPE     -2  /* n != 4, d out of range / not a multiple of the tile, N < 0, iters < 1 */
+#define MHC_ERR_ALIGN     -3  /* a pointer is not 16-byte aligned                                */
+#define MHC_ERR_ALIAS     -4  /* an output overlaps an input or another output (X_out == X allowed) */
+#define MHC_ERR_CUDA      -5  /* a CUDA runtime/driver call failed (launch, tensor map, attribute) */
+#define MHC_ERR_TIMEOUT   -6  /* a device-side bounded wait gave up (see mhc_get_status)         */
+#define MHC_ERR_WORKSPACE -7  /* workspace missing or smaller than *_workspace_bytes()           */
+
+/* ---- flags ------------------------------------------------------------------------------- */
+/* Reading of comb in hc_post. Default (0): the pages' code, X'_k = u_k F + sum_j C_jk X_j
+ * (Stream weights for the feed-forward, Code: hc_post sums over comb's first stream index).
+ * MHC_COMB_ROW_DEST: X'_j = u_j F + sum_k C_jk X_k (element (i,j) = "from stream j into stream i",
+ * "2A · Single-Pass mHC", section 3).                                                        */
+#define MHC_COMB_ROW_DEST        0x1u
+/* Test hook: one thread per CTA waits on a barrier that nothing completes, with a ~2 ms limit;
+ * the wait gives up, records MHC_ERR_TIMEOUT for mhc_get_status, and the call completes.      */
+#define MHC_DEBUG_NEVER_ARRIVE   0x2u
+/* Bits 8..11: number of CTAs (1, 2, 4 or 8) that split the width d of each token tile between
+ * them (a thread-block cluster). 0 = automatic (the fewest that fit on chip).                  */
+#define MHC_SPLIT_SHIFT          8
+#define MHC_SPLIT_MASK           (0xFu << MHC_SPLIT_SHIFT)
+
+/* ---- sizes ------------------------------------------------------------------------------- */
+/* Bytes of the packed projection weights: 3 bf16 planes of W_mix, [3*(2+n)*n, n*d].           */
+size_t mhc_packed_weights_bytes(int n, int d);
+/* Workspace of mhc_fused_step / mhc_mixes (the packed weights).                              */
+size_t mhc_workspace_bytes(int n, int d);
+
+/* ---- the fused single-pass step ------------------------------------------------------------
+ * One sublayer of the single-pass mHC step (MoE RMSNorm, Code: Block.forward, FFN half;
+ * Stream weights for the feed-forward, "Why" and "All 5 steps"), in ONE kernel pass over the
+ * streams:
+ *   X'   = hc_post(X, F, post_prev, comb_prev)                  -> X_out  (bf16, rounded)
+ *   m    = (flatten(X') W_mix^T) / sqrt(mean(flatten(X')^2) + norm_eps)      -> mixes_out
+ *   pre  = sigmoid(scale[0] m[0:n] + base[0:n]) + hc_eps                     -> pre_out
+ *   post = 2 sigmoid(scale[1] m[n:2n] + base[n:2n])                          -> post_out
+ *   comb = Sinkhorn(softmax_k(scale[2] m[2n:] + base[2n:]) ), sinkhorn_iters rounds -> comb_out
+ *   y    = RMSNorm(hc_pre(X', pre_prev); gain, norm_eps)                     -> y_out (bf16)
+ * hc_post and hc_pre are evaluated in float32 (Code: hc_post, hc_pre) as chains of fused
+ * multiply-adds over the stream index, left to right, then rounded to bf16:
+ *   X'_k  = fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0))))
+ *   y_hat = fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0)))
+ *
+ *   X         bf16 [N, n, d]      residual streams                      (read once)
+ *   F         bf16 [N, d]         sublayer output                        (read once)
+ *   pre_prev  fp32 [N, n]         previous reading weights (used by hc_pre)
+ *   post_prev fp32 [N, n]         previous writing weights (used by hc_post)
+ *   comb_prev fp32 [N, n, n]      previous stream combination (used by hc_post)
+ *   W_mix     fp32 [(2+n)n, n*d]  projection, flat index k*d + i (stream-major)
+ *   scale     fp32 [3], base fp32 [(2+n)n], gain fp32 [d]
+ *   X_out     bf16 [N, n, d]      may equal X (in place); no other overlap
+ *   y_out     bf16 [N, d]
+ *   pre_out, post_out fp32 [N, n]; comb_out fp32 [N, n, n]; mixes_out fp32 [N, (2+n)n] or NULL
+ *   d: multiple of 32*split and d/split <= 768 for the chosen split (d = 5120 uses split 8).
+ *   workspace: >= mhc_workspace_bytes(n, d) device bytes; W_mix is packed into it each call.
+ * Returns MHC_OK or a negative code. N == 0 returns MHC_OK once the shape is valid, without
+ * looking at the pointers (empty tensors may have none) and without launching.               */
+int mhc_fused_step(const void* X, const void* F, const float* pre_prev, const float* post_prev,
+                   const float* comb_prev, const float* W_mix, const float* scale,
+                   const float* base, const float* gain, void* X_out, void* y_out,
+                   float* pre_out, float* post_out, float* comb_out, float* mixes_out,
+                   int64_t N, int n, int d, int sinkhorn_iters, float hc_eps, float norm_eps,
+                   unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same step with W_mix already packed by mhc_pack_weights (no per-call packing).             */
+int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
+                          const float* post_prev, const float* comb_prev, const void* W_packed,
+                          const float* scale, const float* base, const float* gain, void* X_out,
+                          void* y_out, float* pre_out, float* post_out, float* comb_out,
+                          float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
+                          float hc_eps, float norm_eps, unsigned flags, void* stream);
+
+/* ---- hc_mixes alone ------------------------------------------------------------------------
+ * Stream weights for the feed-forward, Code: hc_mixes (+ the hc_split_sinkhorn kernel): from
+ * bf16 streams X [N,n,d], the 24 mix numbers m (optional output) and pre/post/comb as above.
+ * Same shape rules and workspace as mhc_fused_step.                                          */
+int mhc_mixes(const void* X, const float* W_mix, const float* scale, const float* base,
+              float* mixes_out, float* pre_out, float* post_out, float* comb_out, int64_t N,
+              int n, int d, int sinkhorn_iters, float hc_eps, float norm_eps, unsigned flags,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- split + Sinkhorn alone ----------------------------------------------------------------
+ * Stream weights for the feed-forward, Code: hc_split_sinkhorn kernel. mixes fp32 [N,(2+n)n]
+ * -> pre, post fp32 [N,n], comb fp32 [N,n,n]. Any N >= 0, sinkhorn_iters >= 1.            */
+int mhc_sinkhorn(const float* mixes, const float* scale, const float* base, float* pre_out,
+                 float* post_out, float* comb_out, int64_t N, int n, int sinkhorn_iters,
+                 float hc_eps, void* stream);
+
+/* ---- RMSNorm alone -------------------------------------------------------------------------
+ * MoE RMSNorm, formula block and Code: RMSNorm. x bf16 [N,d] -> y = bf16(gain * x /
+ * sqrt(mean(x^2) + eps)) [N,d]. d multiple of 8; y may equal x.                              */
+int mhc_rmsnorm(const void* x, const float* gain, void* y, int64_t N, int d, float eps,
+                void* stream);
+
+/* ---- the unfused form, one op per kernel ---------------------------------------------------
+ * The earlier form the page "Stream weights for the feed-forward" ("Why") compares against:
+ * hc_post, hc_mixes and hc_pre as separate kernels (plus RMSNorm), each a full pass over the
+ * streams. Same arithmetic as the fused step; used to measure the (4n+4)d vs (2n+2)d traffic.
+ * mhc_hc_post: X, F, post, comb -> X_out bf16 [N,n,d] (flags: MHC_COMB_ROW_DEST).
+ * mhc_hc_pre:  X' bf16 [N,n,d], pre fp32 [N,n] -> y_hat bf16 [N,d].  d multiple of 8.        */
+int mhc_hc_post(const void* X, const void* F, const float* post, const float* comb, void* X_out,
+                int64_t N, int n, int d, unsigned flags, void* stream);
+int mhc_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int n, int d,
+               void* stream);
+
+/* ---- weights packing -----------------------------------------------------------------------
+ * Split fp32 W_mix [(2+n)n, n*d] into three bf16 planes hi + mid + lo (each the bf16 rounding
+ * of what the previous planes left), stored as packed [3*(2+n)n, n*d]: rows 0..23 hi,
+ * 24..47 mid, 48..71 lo. The three planes carry W to float32 accuracy for the tensor cores.   */
+int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* stream);
+
+/* ---- status --------------------------------------------------------------------------------
+ * Synchronises `stream`, then returns and clears the device status word: MHC_OK, or
+ * MHC_ERR_TIMEOUT if a bounded device-side wait gave up since the last call, or MHC_ERR_CUDA
+ * if the synchronisation itself failed.                                                       */
+int mhc_get_status(void* stream);
+/* Launch shape of the fused step on the current device: the width split it uses for (n, d,
+ * flags) and how many such clusters the device can hold at once (cudaOccupancyMaxActiveClusters).
+ * Diagnostic only; needs a GPU.                                                               */
+int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters);
+/* Static text for a status code.                                                              */
+const char* mhc_strerror(int code);
+/* Library ABI version (major*100 + minor).                                                    */
+int mhc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MHC_H */

@@ -1,0 +1,331 @@
+// abi.cu -- the exported C ABI: argument validation, launches, status word.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "mhc.h"
+
+namespace mhc {
+namespace {
+
+// The status word: set by device-side bounded waits that give up, read and cleared by
+// mhc_get_status. One per device that loaded the library (static, never allocated).
+__device__ unsigned g_status;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+  uintptr_t lo, hi;
+  bool empty() const { return hi <= lo; }
+};
+Span span(const void* p, uint64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Span{a, a + static_cast<uintptr_t>(bytes)};
+}
+bool overlap(Span a, Span b) { return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi; }
+
+// Outputs must not overlap inputs or each other; (out i, in j) pairs listed in `same_ok` may be
+// exactly equal (same start and size).
+template <int NO, int NI>
+bool aliasing_ok(const Span (&outs)[NO], const Span (&ins)[NI], int same_out = -1, int same_in = -1) {
+  for (int i = 0; i < NO; ++i) {
+    for (int j = 0; j < NI; ++j) {
+      if (i == same_out && j == same_in && outs[i].lo == ins[j].lo && outs[i].hi == ins[j].hi) continue;
+      if (overlap(outs[i], ins[j])) return false;
+    }
+    for (int j = i + 1; j < NO; ++j)
+      if (overlap(outs[i], outs[j])) return false;
+  }
+  return true;
+}
+
+int cuda_code(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
+
+}  // namespace
+
+unsigned* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+}  // namespace mhc
+
+using namespace mhc;
+
+namespace {
+
+// Checks shared by the fused step and the mixes call. Returns MHC_OK and the split, or a code.
+int check_step_shape(int64_t N, int n, int d, int iters, unsigned flags, int* split) {
+  if (n != 4 || N < 0 || N > kMaxTokens || iters < 1 || d <= 0) return MHC_ERR_SHAPE;
+  const int forced = static_cast<int>((flags & MHC_SPLIT_MASK) >> MHC_SPLIT_SHIFT);
+  *split = choose_split(d, forced);
+  return *split == 0 ? MHC_ERR_SHAPE : MHC_OK;
+}
+
+int fused_common(const void* X, const void* F, const float* pre_prev, const float* post_prev,
+                 const float* comb_prev, const void* W_packed, const float* scale,
+                 const float* base, const float* gain, void* X_out, void* y_out, float* pre_out,
+                 float* post_out, float* comb_out, float* mixes_out, int64_t N, int n, int d,
+                 int iters, float hc_eps, float norm_eps, unsigned flags, const void* workspace,
+                 uint64_t ws_bytes, const float* W_mix, void* stream) {
+  int split = 0;
+  int rc = check_step_shape(N, n, d, iters, flags, &split);
+  if (rc != MHC_OK) return rc;
+  if (N == 0) return MHC_OK;  // nothing to read or write (empty tensors may have no address)
+  if (!X || !F || !pre_prev || !post_prev || !comb_prev || !W_packed || !scale || !base || !gain ||
+      !X_out || !y_out || !pre_out || !post_out || !comb_out)
+    return MHC_ERR_NULL;
+  const void* ptrs[] = {X, F, pre_prev, post_prev, comb_prev, W_packed, scale, base, gain,
+                        X_out, y_out, pre_out, post_out, comb_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MHC_ERR_ALIGN;
+  if (mixes_out && !aligned16(mixes_out)) return MHC_ERR_ALIGN;
+  if (W_mix && !aligned16(W_mix)) return MHC_ERR_ALIGN;
+
+  const uint64_t nt = static_cast<uint64_t>(N);
+  const uint64_t K = 4ull * d;
+  const Span ins[] = {span(X, nt * K * 2),     span(F, nt * d * 2),      span(pre_prev, nt * 16),
+                      span(post_prev, nt * 16), span(comb_prev, nt * 64), span(scale, 12),
+                      span(base, 96),          span(gain, 4ull * d),     span(W_mix, W_mix ? 96 * K : 0)};
+  const Span outs[] = {span(X_out, nt * K * 2), span(y_out, nt * d * 2), span(pre_out, nt * 16),
+                       span(post_out, nt * 16), span(comb_out, nt * 64),
+                       span(mixes_out, mixes_out ? nt * 96 : 0),
+                       span(workspace, workspace ? ws_bytes : 0)};
+  if (!aliasing_ok(outs, ins, 0, 0)) return MHC_ERR_ALIAS;
+  if (!workspace) {  // pre-packed weights are an input too
+    const Span packed_in[] = {span(W_packed, 144 * K)};
+    if (!aliasing_ok(outs, packed_in)) return MHC_ERR_ALIAS;
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (W_mix) {
+    rc = cuda_code(launch_pack(W_mix, const_cast<void*>(W_packed), d, s));
+    if (rc != MHC_OK) return rc;
+  }
+  StepArgs a{};
+  a.X = X;
+  a.F = F;
+  a.pre_prev = pre_prev;
+  a.post_prev = post_prev;
+  a.comb_prev = comb_prev;
+  a.W_packed = W_packed;
+  a.scale = scale;
+  a.base = base;
+  a.gain = gain;
+  a.X_out = X_out;
+  a.y_out = y_out;
+  a.pre_out = pre_out;
+  a.post_out = post_out;
+  a.comb_out = comb_out;
+  a.mixes_out = mixes_out;
+  a.N = N;
+  a.d = d;
+  a.split = split;
+  a.iters = iters;
+  a.hc_eps = hc_eps;
+  a.norm_eps = norm_eps;
+  a.flags = flags;
+  return cuda_code(launch_step(true, a, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mhc_packed_weights_bytes(int n, int d) {
+  if (n != 4 || d <= 0) return 0;
+  return static_cast<size_t>(3) * (2 + n) * n * static_cast<size_t>(n) * d * 2;
+}
+
+size_t mhc_workspace_bytes(int n, int d) { return mhc_packed_weights_bytes(n, d); }
+
+int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* stream) {
+  if (!W_mix || !W_packed) return MHC_ERR_NULL;
+  if (n != 4 || d <= 0 || d % 8 != 0) return MHC_ERR_SHAPE;
+  if (!aligned16(W_mix) || !aligned16(W_packed)) return MHC_ERR_ALIGN;
+  const uint64_t K = 4ull * d;
+  if (overlap(span(W_mix, 96 * K), span(W_packed, 144 * K))) return MHC_ERR_ALIAS;
+  return cuda_code(launch_pack(W_mix, W_packed, d, static_cast<cudaStream_t>(stream)));
+}
+
+int mhc_fused_step(const void* X, const void* F, const float* pre_prev, const float* post_prev,
+                   const float* comb_prev, const float* W_mix, const float* scale,
+                   const float* base, const float* gain, void* X_out, void* y_out,
+                   float* pre_out, float* post_out, float* comb_out, float* mixes_out,
+                   int64_t N, int n, int d, int sinkhorn_iters, float hc_eps, float norm_eps,
+                   unsigned flags, void* workspace, size_t workspace_bytes, void* stream) {
+  int split = 0;
+  const int rc = check_step_shape(N, n, d, sinkhorn_iters, flags, &split);
+  if (rc != MHC_OK) return rc;
+  if (N == 0) return MHC_OK;
+  if (!W_mix) return MHC_ERR_NULL;
+  if (!workspace || workspace_bytes < mhc_workspace_bytes(n, d)) return MHC_ERR_WORKSPACE;
+  return fused_common(X, F, pre_prev, post_prev, comb_prev, workspace, scale, base, gain, X_out,
+                      y_out, pre_out, post_out, comb_out, mixes_out, N, n, d, sinkhorn_iters,
+                      hc_eps, norm_eps, flags, workspace, workspace_bytes, W_mix, stream);
+}
+
+int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
+                          const float* post_prev, const float* comb_prev, const void* W_packed,
+                          const float* scale, const float* base, const float* gain, void* X_out,
+                          void* y_out, float* pre_out, float* post_out, float* comb_out,
+                          float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
+                          float hc_eps, float norm_eps, unsigned flags, void* stream) {
+  return fused_common(X, F, pre_prev, post_prev, comb_prev, W_packed, scale, base, gain, X_out,
+                      y_out, pre_out, post_out, comb_out, mixes_out, N, n, d, sinkhorn_iters,
+                      hc_eps, norm_eps, flags, nullptr, 0, nullptr, stream);
+}
+
+int mhc_mixes(const void* X, const float* W_mix, const float* scale, const float* base,
+              float* mixes_out, float* pre_out, float* post_out, float* comb_out, int64_t N,
+              int n, int d, int sinkhorn_iters, float hc_eps, float norm_eps, unsigned flags,
+              void* workspace, size_t workspace_bytes, void* stream) {
+  int split = 0;
+  int rc = check_step_shape(N, n, d, sinkhorn_iters, flags, &split);
+  if (rc != MHC_OK) return rc;
+  if (N == 0) return MHC_OK;
+  if (!X || !W_mix || !scale || !base || !pre_out || !post_out || !comb_out) return MHC_ERR_NULL;
+  if (!workspace) return MHC_ERR_WORKSPACE;
+  if (workspace_bytes < mhc_workspace_bytes(n, d)) return MHC_ERR_WORKSPACE;
+  const void* ptrs[] = {X, W_mix, scale, base, pre_out, post_out, comb_out, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MHC_ERR_ALIGN;
+  if (mixes_out && !aligned16(mixes_out)) return MHC_ERR_ALIGN;
+  const uint64_t nt = static_cast<uint64_t>(N), K = 4ull * d;
+  const Span ins[] = {span(X, nt * K * 2), span(W_mix, 96 * K), span(scale, 12), span(base, 96)};
+  const Span outs[] = {span(pre_out, nt * 16), span(post_out, nt * 16), span(comb_out, nt * 64),
+                       span(mixes_out, mixes_out ? nt * 96 : 0), span(workspace, workspace_bytes)};
+  if (!aliasing_ok(outs, ins)) return MHC_ERR_ALIAS;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = cuda_code(launch_pack(W_mix, workspace, d, s));
+  if (rc != MHC_OK) return rc;
+  StepArgs a{};
+  a.X = X;
+  a.W_packed = workspace;
+  a.scale = scale;
+  a.base = base;
+  a.pre_out = pre_out;
+  a.post_out = post_out;
+  a.comb_out = comb_out;
+  a.mixes_out = mixes_out;
+  a.N = N;
+  a.d = d;
+  a.split = split;
+  a.iters = sinkhorn_iters;
+  a.hc_eps = hc_eps;
+  a.norm_eps = norm_eps;
+  a.flags = flags;
+  return cuda_code(launch_step(false, a, s));
+}
+
+int mhc_sinkhorn(const float* mixes, const float* scale, const float* base, float* pre_out,
+                 float* post_out, float* comb_out, int64_t N, int n, int sinkhorn_iters,
+                 float hc_eps, void* stream) {
+  if (n != 4 || N < 0 || sinkhorn_iters < 1 || N > (int64_t(1) << 40)) return MHC_ERR_SHAPE;
+  if (N == 0) return MHC_OK;
+  if (!mixes || !scale || !base || !pre_out || !post_out || !comb_out) return MHC_ERR_NULL;
+  const void* ptrs[] = {mixes, scale, base, pre_out, post_out, comb_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MHC_ERR_ALIGN;
+  const uint64_t nt = static_cast<uint64_t>(N);
+  const Span ins[] = {span(mixes, nt * 96), span(scale, 12), span(base, 96)};
+  const Span outs[] = {span(pre_out, nt * 16), span(post_out, nt * 16), span(comb_out, nt * 64)};
+  if (!aliasing_ok(outs, ins)) return MHC_ERR_ALIAS;
+  return cuda_code(launch_sinkhorn(mixes, scale, base, pre_out, post_out, comb_out, N,
+                                   sinkhorn_iters, hc_eps, static_cast<cudaStream_t>(stream)));
+}
+
+int mhc_rmsnorm(const void* x, const float* gain, void* y, int64_t N, int d, float eps,
+                void* stream) {
+  if (N < 0 || d <= 0 || d % 8 != 0) return MHC_ERR_SHAPE;
+  if (N == 0) return MHC_OK;
+  if (!x || !gain || !y) return MHC_ERR_NULL;
+  if (!aligned16(x) || !aligned16(gain) || !aligned16(y)) return MHC_ERR_ALIGN;
+  const uint64_t nt = static_cast<uint64_t>(N);
+  const Span ins[] = {span(x, nt * d * 2), span(gain, 4ull * d)};
+  const Span outs[] = {span(y, nt * d * 2)};
+  if (!aliasing_ok(outs, ins, 0, 0)) return MHC_ERR_ALIAS;
+  return cuda_code(launch_rmsnorm(x, gain, y, N, d, eps, static_cast<cudaStream_t>(stream)));
+}
+
+int mhc_hc_post(const void* X, const void* F, const float* post, const float* comb, void* X_out,
+                int64_t N, int n, int d, unsigned flags, void* stream) {
+  if (n != 4 || N < 0 || d <= 0 || d % 8 != 0) return MHC_ERR_SHAPE;
+  if (N == 0) return MHC_OK;
+  if (!X || !F || !post || !comb || !X_out) return MHC_ERR_NULL;
+  const void* ptrs[] = {X, F, post, comb, X_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MHC_ERR_ALIGN;
+  const uint64_t nt = static_cast<uint64_t>(N), K = 4ull * d;
+  const Span ins[] = {span(X, nt * K * 2), span(F, nt * d * 2), span(post, nt * 16), span(comb, nt * 64)};
+  const Span outs[] = {span(X_out, nt * K * 2)};
+  if (!aliasing_ok(outs, ins, 0, 0)) return MHC_ERR_ALIAS;
+  return cuda_code(launch_hc_post(X, F, post, comb, X_out, N, d, (flags & MHC_COMB_ROW_DEST) != 0,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int mhc_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int n, int d,
+               void* stream) {
+  if (n != 4 || N < 0 || d <= 0 || d % 8 != 0) return MHC_ERR_SHAPE;
+  if (N == 0) return MHC_OK;
+  if (!Xp || !pre || !y_hat) return MHC_ERR_NULL;
+  if (!aligned16(Xp) || !aligned16(pre) || !aligned16(y_hat)) return MHC_ERR_ALIGN;
+  const uint64_t nt = static_cast<uint64_t>(N);
+  const Span ins[] = {span(Xp, nt * 8ull * d), span(pre, nt * 16)};
+  const Span outs[] = {span(y_hat, nt * d * 2)};
+  if (!aliasing_ok(outs, ins)) return MHC_ERR_ALIAS;
+  return cuda_code(launch_hc_pre(Xp, pre, y_hat, N, d, static_cast<cudaStream_t>(stream)));
+}
+
+int mhc_get_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MHC_ERR_CUDA;
+  unsigned* p = status_word();
+  if (p == nullptr) return MHC_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MHC_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MHC_ERR_CUDA;
+  }
+  return (v & STATUS_TIMEOUT) ? MHC_ERR_TIMEOUT : MHC_OK;
+}
+
+const char* mhc_strerror(int code) {
+  switch (code) {
+    case MHC_OK: return "ok";
+    case MHC_ERR_NULL: return "a required pointer is NULL";
+    case MHC_ERR_SHAPE: return "unsupported shape (n must be 4; d, N or sinkhorn_iters out of range)";
+    case MHC_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case MHC_ERR_ALIAS: return "an output overlaps an input or another output";
+    case MHC_ERR_CUDA: return "a CUDA call failed";
+    case MHC_ERR_TIMEOUT: return "a device-side bounded wait gave up";
+    case MHC_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status code";
+  }
+}
+
+int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters) {
+  if (!split || !clusters) return MHC_ERR_NULL;
+  int sp = 0;
+  const int rc = check_step_shape(0, n, d, 1, flags, &sp);
+  if (rc != MHC_OK) return rc;
+  *split = sp;
+  return cuda_code(step_occupancy(sp, clusters));
+}
+
+int mhc_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mhc {
+
+// Device address of the library's status word on the current device (see mhc_get_status).
+unsigned* status_word();
+
+constexpr unsigned STATUS_TIMEOUT = 1u;
+
+struct StepArgs {
+  const void* X;
+  const void* F;            // fused step only
+  const float* pre_prev;    // fused step only
+  const float* post_prev;   // fused step only
+  const float* comb_prev;   // fused step only
+  const void* W_packed;     // bf16 [72, 4d]
+  const float* scale;
+  const float* base;
+  const float* gain;        // fused step only
+  void* X_out;              // fused step only
+  void* y_out;              // fused step only
+  float* pre_out;
+  float* post_out;
+  float* comb_out;
+  float* mixes_out;         // nullable
+  int64_t N;
+  int d;
+  int split;                // CTAs per token tile (cluster size)
+  int iters;
+  float hc_eps;
+  float norm_eps;
+  unsigned flags;
+};
+
+// Returns the split (1, 2, 4 or 8) the step kernel uses for width d, or 0 if d is not supported.
+// `forced` = 0 picks automatically.
+int choose_split(int d, int forced);
+constexpr int kMaxTokens = 65535 * 128;
+
+cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream);
+cudaError_t step_occupancy(int split, int* clusters);
+cudaError_t launch_pack(const float* W, void* packed, int d, cudaStream_t stream);
+cudaError_t launch_sinkhorn(const float* mixes, const float* scale, const float* base, float* pre,
+                            float* post, float* comb, int64_t N, int iters, float eps,
+                            cudaStream_t stream);
+cudaError_t launch_rmsnorm(const void* x, const float* gain, void* y, int64_t N, int d, float eps,
+                           cudaStream_t stream);
+cudaError_t launch_hc_post(const void* X, const void* F, const float* post, const float* comb,
+                           void* X_out, int64_t N, int d, bool row_dest, cudaStream_t stream);
+cudaError_t launch_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int d,
+                          cudaStream_t stream);
+
+}  // namespace mhc

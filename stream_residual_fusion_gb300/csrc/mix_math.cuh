@@ -1,0 +1,68 @@
+// mix_math.cuh -- per-token split of the 24 mix numbers and the 4x4 Sinkhorn, in registers.
+//
+// Stream weights for the feed-forward, "All 5 steps" and Code: hc_split_sinkhorn kernel:
+//   p_j  = sigmoid(s_0 m_j + b_j) + eps
+//   u_j  = 2 sigmoid(s_1 m_{4+j} + b_{4+j})
+//   L_jk = s_2 m_{8+4j+k} + b_{8+4j+k}
+//   C    = softmax over k (max subtracted) + eps; columns / (sum + eps);
+//          then (iters-1) x [rows / (sum + eps), columns / (sum + eps)].
+// One thread owns one token. Divisions by a row or column sum are a correctly rounded
+// reciprocal followed by a multiply (4 reciprocals instead of 16 divisions per step).
+#pragma once
+
+namespace mhc {
+
+__device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void split_sinkhorn(const float (&m)[24], float s0, float s1, float s2,
+                                               const float* __restrict__ base, int iters,
+                                               float eps, float (&p)[4], float (&u)[4],
+                                               float (&c)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    p[j] = sigmoid_f(fmaf(m[j], s0, __ldg(base + j))) + eps;
+    u[j] = 2.0f * sigmoid_f(fmaf(m[4 + j], s1, __ldg(base + 4 + j)));
+  }
+#pragma unroll
+  for (int jk = 0; jk < 16; ++jk) c[jk] = fmaf(m[8 + jk], s2, __ldg(base + 8 + jk));
+
+  // row softmax, then + eps
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float mx = fmaxf(fmaxf(c[4 * j], c[4 * j + 1]), fmaxf(c[4 * j + 2], c[4 * j + 3]));
+    float e0 = expf(c[4 * j] - mx), e1 = expf(c[4 * j + 1] - mx);
+    float e2 = expf(c[4 * j + 2] - mx), e3 = expf(c[4 * j + 3] - mx);
+    float r = __frcp_rn((e0 + e1) + (e2 + e3));
+    c[4 * j] = fmaf(e0, r, eps);
+    c[4 * j + 1] = fmaf(e1, r, eps);
+    c[4 * j + 2] = fmaf(e2, r, eps);
+    c[4 * j + 3] = fmaf(e3, r, eps);
+  }
+  auto col_step = [&]() {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float r = __frcp_rn(((c[k] + c[4 + k]) + (c[8 + k] + c[12 + k])) + eps);
+      c[k] *= r;
+      c[4 + k] *= r;
+      c[8 + k] *= r;
+      c[12 + k] *= r;
+    }
+  };
+  auto row_step = [&]() {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float r = __frcp_rn(((c[4 * j] + c[4 * j + 1]) + (c[4 * j + 2] + c[4 * j + 3])) + eps);
+      c[4 * j] *= r;
+      c[4 * j + 1] *= r;
+      c[4 * j + 2] *= r;
+      c[4 * j + 3] *= r;
+    }
+  };
+  col_step();
+  for (int it = 1; it < iters; ++it) {
+    row_step();
+    col_step();
+  }
+}
+
+}  // namespace mhc

@@ -1,0 +1,246 @@
+// small.cu -- the standalone kernels: weight packing, split + Sinkhorn, RMSNorm, and the
+// one-op-per-kernel hc_post / hc_pre of the unfused form.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "mix_math.cuh"
+#include "ptx.cuh"
+
+namespace mhc {
+namespace {
+
+// W fp32 [24, K] -> bf16 [72, K]: rows r, 24+r, 48+r hold hi, mid, lo with
+// hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid). The differences are exact in fp32.
+__global__ void pack_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ P, int64_t K) {
+  const int64_t total = 24 * K;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = idx / K, col = idx - r * K;
+    const float w = W[idx];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float rem1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(rem1);
+    const float rem2 = rem1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(rem2);
+    P[r * K + col] = hi;
+    P[(24 + r) * K + col] = mid;
+    P[(48 + r) * K + col] = lo;
+  }
+}
+
+// One thread per token (Stream weights for the feed-forward, Code: hc_split_sinkhorn kernel).
+__global__ void sinkhorn_kernel(const float* __restrict__ mixes, const float* __restrict__ scale,
+                                const float* __restrict__ base, float* __restrict__ pre,
+                                float* __restrict__ post, float* __restrict__ comb, int64_t N,
+                                int iters, float eps) {
+  const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (t >= N) return;
+  float m[24];
+  const float4* src = reinterpret_cast<const float4*>(mixes + t * 24);
+#pragma unroll
+  for (int r = 0; r < 6; ++r) {
+    const float4 v = __ldg(src + r);
+    m[4 * r] = v.x;
+    m[4 * r + 1] = v.y;
+    m[4 * r + 2] = v.z;
+    m[4 * r + 3] = v.w;
+  }
+  float p[4], u[4], c[16];
+  split_sinkhorn(m, __ldg(scale), __ldg(scale + 1), __ldg(scale + 2), base, iters, eps, p, u, c);
+  reinterpret_cast<float4*>(pre)[t] = make_float4(p[0], p[1], p[2], p[3]);
+  reinterpret_cast<float4*>(post)[t] = make_float4(u[0], u[1], u[2], u[3]);
+  float4* co = reinterpret_cast<float4*>(comb + t * 16);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) co[r] = make_float4(c[4 * r], c[4 * r + 1], c[4 * r + 2], c[4 * r + 3]);
+}
+
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += scratch[i];
+  __syncthreads();
+  return t;
+}
+
+// One block per row (MoE RMSNorm, Code: RMSNorm): sum of squares in fp32, then
+// y = bf16(gain * (x * rsqrt(mean + eps))).
+__global__ void rmsnorm_kernel(const uint4* __restrict__ x, const float* __restrict__ gain,
+                               uint4* __restrict__ y, int64_t N, int d, float eps) {
+  __shared__ float scratch[32];
+  const int chunks = d / 8;
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+    const uint4* xr = x + row * chunks;
+    f2 acc{0.f, 0.f};
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = xr[c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const f2 a = bf2_to_f2(w[e]);
+        acc = fma2(a, a, acc);
+      }
+    }
+    const float ss = block_sum(acc.x + acc.y, scratch);
+    const float r = rsqrtf(__fdiv_rn(ss, static_cast<float>(d)) + eps);
+    const f2 r2{r, r};
+    uint4* yr = y + row * chunks;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const uint4 v = xr[c];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * c);
+      const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain) + 2 * c + 1);
+      const f2 gp[4] = {f2{g0.x, g0.y}, f2{g0.z, g0.w}, f2{g1.x, g1.y}, f2{g1.z, g1.w}};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = f2_to_bf2(mul2(gp[e], mul2(bf2_to_f2(w[e]), r2)));
+      yr[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// hc_post alone: one thread per 8 columns of one token, all 4 streams (same float32 order as
+// the fused kernel: X'_k = fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0))))).
+__global__ void hc_post_kernel(const uint4* __restrict__ X, const uint4* __restrict__ F,
+                               const float* __restrict__ post, const float* __restrict__ comb,
+                               uint4* __restrict__ Xo, int64_t N, int d, int row_dest) {
+  const int chunks = d / 8;
+  const int64_t total = N * chunks;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = idx / chunks;
+    const int c = static_cast<int>(idx - t * chunks);
+    f2 cu[4], cc[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float uk = __ldg(post + t * 4 + k);
+      cu[k] = f2{uk, uk};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float v = __ldg(comb + t * 16 + (row_dest ? k * 4 + j : j * 4 + k));
+        cc[j][k] = f2{v, v};
+      }
+    }
+    const uint4 fv = F[t * chunks + c];
+    uint4 xv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) xv[j] = X[(t * 4 + j) * chunks + c];
+    const uint32_t fw[4] = {fv.x, fv.y, fv.z, fv.w};
+    uint32_t ow[4][4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const f2 f = bf2_to_f2(fw[w]);
+      f2 x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        x[j] = bf2_to_f2(xw[w]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        f2 mixed = mul2(cc[0][k], x[0]);
+        mixed = fma2(cc[1][k], x[1], mixed);
+        mixed = fma2(cc[2][k], x[2], mixed);
+        mixed = fma2(cc[3][k], x[3], mixed);
+        ow[k][w] = f2_to_bf2(fma2(cu[k], f, mixed));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) Xo[(t * 4 + k) * chunks + c] = make_uint4(ow[k][0], ow[k][1], ow[k][2], ow[k][3]);
+  }
+}
+
+// hc_pre alone: y_hat = bf16(fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0)))).
+__global__ void hc_pre_kernel(const uint4* __restrict__ Xp, const float* __restrict__ pre,
+                              uint4* __restrict__ y, int64_t N, int d) {
+  const int chunks = d / 8;
+  const int64_t total = N * chunks;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = idx / chunks;
+    const int c = static_cast<int>(idx - t * chunks);
+    f2 cp[4];
+    uint4 xv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float pj = __ldg(pre + t * 4 + j);
+      cp[j] = f2{pj, pj};
+      xv[j] = Xp[(t * 4 + j) * chunks + c];
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      f2 x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        x[j] = bf2_to_f2(xw[w]);
+      }
+      f2 yh = mul2(cp[0], x[0]);
+      yh = fma2(cp[1], x[1], yh);
+      yh = fma2(cp[2], x[2], yh);
+      yh = fma2(cp[3], x[3], yh);
+      o[w] = f2_to_bf2(yh);
+    }
+    y[t * chunks + c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const float* W, void* packed, int d, cudaStream_t stream) {
+  const int64_t K = 4 * static_cast<int64_t>(d);
+  pack_kernel<<<grid_for(24 * K, 256), 256, 0, stream>>>(W, static_cast<__nv_bfloat16*>(packed), K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sinkhorn(const float* mixes, const float* scale, const float* base, float* pre,
+                            float* post, float* comb, int64_t N, int iters, float eps,
+                            cudaStream_t stream) {
+  const int threads = 128;
+  const int64_t blocks = (N + threads - 1) / threads;
+  sinkhorn_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(mixes, scale, base, pre,
+                                                                         post, comb, N, iters, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const void* x, const float* gain, void* y, int64_t N, int d, float eps,
+                           cudaStream_t stream) {
+  const int threads = 256;
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = N < static_cast<int64_t>(sms) * 8 ? N : static_cast<int64_t>(sms) * 8;
+  rmsnorm_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4*>(x), gain, static_cast<uint4*>(y), N, d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hc_post(const void* X, const void* F, const float* post, const float* comb,
+                           void* X_out, int64_t N, int d, bool row_dest, cudaStream_t stream) {
+  const int threads = 256;
+  hc_post_kernel<<<grid_for(N * (d / 8), threads), threads, 0, stream>>>(
+      static_cast<const uint4*>(X), static_cast<const uint4*>(F), post, comb,
+      static_cast<uint4*>(X_out), N, d, row_dest ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int d,
+                          cudaStream_t stream) {
+  const int threads = 256;
+  hc_pre_kernel<<<grid_for(N * (d / 8), threads), threads, 0, stream>>>(
+      static_cast<const uint4*>(Xp), pre, static_cast<uint4*>(y_hat), N, d);
+  return cudaGetLastError();
+}
+
+}  // namespace mhc

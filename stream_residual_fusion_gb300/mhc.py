@@ -1,0 +1,260 @@
+"""ctypes binding of libmhc.so, the GB300 single-pass mHC step.
+
+Argument marshalling only: every step of the computation runs in the library's CUDA kernels.
+PyTorch is used for device memory and streams. If the library is missing or fails to load, the
+import of the binding raises; there is no other code path.
+
+Calls mirror the C ABI in include/mhc.h (same names without the `mhc_` prefix). Tensors must be
+CUDA, contiguous, with the dtypes the header lists; outputs are allocated here with torch unless
+passed in.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmhc.so")
+
+MHC_OK = 0
+MHC_ERR_NULL = -1
+MHC_ERR_SHAPE = -2
+MHC_ERR_ALIGN = -3
+MHC_ERR_ALIAS = -4
+MHC_ERR_CUDA = -5
+MHC_ERR_TIMEOUT = -6
+MHC_ERR_WORKSPACE = -7
+
+COMB_ROW_DEST = 0x1
+DEBUG_NEVER_ARRIVE = 0x2
+SPLIT_SHIFT = 8
+
+N_STREAMS = 4
+MIX = (2 + N_STREAMS) * N_STREAMS
+
+
+class MhcError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {lib.mhc_strerror(code).decode()} ({code})")
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_F = ctypes.c_float
+_U = ctypes.c_uint
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes); the signatures of include/mhc.h
+SIGNATURES = {
+    "mhc_packed_weights_bytes": (_SZ, [_I, _I]),
+    "mhc_workspace_bytes": (_SZ, [_I, _I]),
+    "mhc_fused_step": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
+    "mhc_fused_step_packed": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P]),
+    "mhc_mixes": (_I, [_P] * 8 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
+    "mhc_sinkhorn": (_I, [_P] * 6 + [_I64, _I, _I, _F, _P]),
+    "mhc_rmsnorm": (_I, [_P] * 3 + [_I64, _I, _F, _P]),
+    "mhc_hc_post": (_I, [_P] * 5 + [_I64, _I, _I, _U, _P]),
+    "mhc_hc_pre": (_I, [_P] * 3 + [_I64, _I, _I, _P]),
+    "mhc_pack_weights": (_I, [_P, _P, _I, _I, _P]),
+    "mhc_get_status": (_I, [_P]),
+    "mhc_strerror": (ctypes.c_char_p, [_I]),
+    "mhc_step_occupancy": (_I, [_I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "mhc_version": (_I, []),
+}
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libmhc.so not built at {path}; run __graft_entry__.build()")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+lib = load_library()
+
+
+# ---------------------------------------------------------------------------------------------
+# helpers
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != MHC_OK:
+        raise MhcError(rc, where)
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def split_flag(split: int) -> int:
+    """Flag bits that force the number of CTAs splitting the width (1, 2, 4 or 8)."""
+    return (split & 0xF) << SPLIT_SHIFT
+
+
+def workspace_bytes(d: int, n: int = N_STREAMS) -> int:
+    return int(lib.mhc_workspace_bytes(n, d))
+
+
+def packed_weights_bytes(d: int, n: int = N_STREAMS) -> int:
+    return int(lib.mhc_packed_weights_bytes(n, d))
+
+
+# ---------------------------------------------------------------------------------------------
+# the calls
+
+def pack_weights(W, out=None, stream=None):
+    _need(W, torch.float32, "W")
+    n = N_STREAMS
+    d = W.shape[1] // n
+    if out is None:
+        out = torch.empty(3 * MIX, n * d, dtype=torch.bfloat16, device=W.device)
+    _check(lib.mhc_pack_weights(_ptr(W), _ptr(out), n, d, _stream(stream)), "mhc_pack_weights")
+    return out
+
+
+def _step_outputs(X, out, with_mixes):
+    N, n, d = X.shape
+    dev = X.device
+    out = dict(out or {})
+    out.setdefault("Xp", torch.empty_like(X))
+    out.setdefault("y", torch.empty(N, d, dtype=torch.bfloat16, device=dev))
+    out.setdefault("pre", torch.empty(N, n, dtype=torch.float32, device=dev))
+    out.setdefault("post", torch.empty(N, n, dtype=torch.float32, device=dev))
+    out.setdefault("comb", torch.empty(N, n, n, dtype=torch.float32, device=dev))
+    if with_mixes:
+        out.setdefault("mixes", torch.empty(N, MIX, dtype=torch.float32, device=dev))
+    return out
+
+
+def fused_step(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, iters=20,
+               hc_eps=1e-6, norm_eps=1e-6, flags=0, with_mixes=False, out=None, workspace=None,
+               W_packed=None, stream=None):
+    """One fused single-pass mHC step (mhc_fused_step, or mhc_fused_step_packed when
+    `W_packed` is given). Returns dict with Xp, y, pre, post, comb (and mixes)."""
+    _need(X, torch.bfloat16, "X")
+    _need(F, torch.bfloat16, "F")
+    for t, nm in ((pre_prev, "pre_prev"), (post_prev, "post_prev"), (comb_prev, "comb_prev"),
+                  (scale, "scale"), (base, "base"), (gain, "gain")):
+        _need(t, torch.float32, nm)
+    N, n, d = X.shape
+    o = _step_outputs(X, out, with_mixes)
+    common_out = [_ptr(o["Xp"]), _ptr(o["y"]), _ptr(o["pre"]), _ptr(o["post"]), _ptr(o["comb"]),
+                  _ptr(o.get("mixes"))]
+    if W_packed is not None:
+        _need(W_packed, torch.bfloat16, "W_packed")
+        rc = lib.mhc_fused_step_packed(
+            _ptr(X), _ptr(F), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev), _ptr(W_packed),
+            _ptr(scale), _ptr(base), _ptr(gain), *common_out, N, n, d, iters, hc_eps, norm_eps,
+            flags, _stream(stream))
+        _check(rc, "mhc_fused_step_packed")
+    else:
+        _need(W, torch.float32, "W")
+        if workspace is None:
+            workspace = torch.empty(workspace_bytes(d, n), dtype=torch.uint8, device=X.device)
+        rc = lib.mhc_fused_step(
+            _ptr(X), _ptr(F), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev), _ptr(W),
+            _ptr(scale), _ptr(base), _ptr(gain), *common_out, N, n, d, iters, hc_eps, norm_eps,
+            flags, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+        _check(rc, "mhc_fused_step")
+    return o
+
+
+def mixes(X, W, scale, base, *, iters=20, hc_eps=1e-6, norm_eps=1e-6, flags=0, with_mixes=True,
+          workspace=None, stream=None):
+    """hc_mixes alone (mhc_mixes). Returns dict with pre, post, comb (and mixes)."""
+    _need(X, torch.bfloat16, "X")
+    for t, nm in ((W, "W"), (scale, "scale"), (base, "base")):
+        _need(t, torch.float32, nm)
+    N, n, d = X.shape
+    dev = X.device
+    o = {"pre": torch.empty(N, n, dtype=torch.float32, device=dev),
+         "post": torch.empty(N, n, dtype=torch.float32, device=dev),
+         "comb": torch.empty(N, n, n, dtype=torch.float32, device=dev)}
+    if with_mixes:
+        o["mixes"] = torch.empty(N, MIX, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(d, n), dtype=torch.uint8, device=dev)
+    rc = lib.mhc_mixes(_ptr(X), _ptr(W), _ptr(scale), _ptr(base), _ptr(o.get("mixes")),
+                       _ptr(o["pre"]), _ptr(o["post"]), _ptr(o["comb"]), N, n, d, iters, hc_eps,
+                       norm_eps, flags, _ptr(workspace),
+                       workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mhc_mixes")
+    return o
+
+
+def sinkhorn(mixes_, scale, base, *, iters=20, hc_eps=1e-6, stream=None):
+    """Split + Sinkhorn alone (mhc_sinkhorn). Returns dict with pre, post, comb."""
+    for t, nm in ((mixes_, "mixes"), (scale, "scale"), (base, "base")):
+        _need(t, torch.float32, nm)
+    N = mixes_.shape[0]
+    n = N_STREAMS
+    dev = mixes_.device
+    o = {"pre": torch.empty(N, n, dtype=torch.float32, device=dev),
+         "post": torch.empty(N, n, dtype=torch.float32, device=dev),
+         "comb": torch.empty(N, n, n, dtype=torch.float32, device=dev)}
+    rc = lib.mhc_sinkhorn(_ptr(mixes_), _ptr(scale), _ptr(base), _ptr(o["pre"]), _ptr(o["post"]),
+                          _ptr(o["comb"]), N, n, iters, hc_eps, _stream(stream))
+    _check(rc, "mhc_sinkhorn")
+    return o
+
+
+def rmsnorm(x, gain, eps=1e-6, out=None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    _need(gain, torch.float32, "gain")
+    N, d = x.shape
+    y = torch.empty_like(x) if out is None else out
+    _check(lib.mhc_rmsnorm(_ptr(x), _ptr(gain), _ptr(y), N, d, eps, _stream(stream)), "mhc_rmsnorm")
+    return y
+
+
+def hc_post(X, F, post, comb, flags=0, out=None, stream=None):
+    _need(X, torch.bfloat16, "X")
+    _need(F, torch.bfloat16, "F")
+    N, n, d = X.shape
+    Xo = torch.empty_like(X) if out is None else out
+    _check(lib.mhc_hc_post(_ptr(X), _ptr(F), _ptr(post), _ptr(comb), _ptr(Xo), N, n, d, flags,
+                           _stream(stream)), "mhc_hc_post")
+    return Xo
+
+
+def hc_pre(Xp, pre, out=None, stream=None):
+    _need(Xp, torch.bfloat16, "Xp")
+    _need(pre, torch.float32, "pre")
+    N, n, d = Xp.shape
+    y = torch.empty(N, d, dtype=torch.bfloat16, device=Xp.device) if out is None else out
+    _check(lib.mhc_hc_pre(_ptr(Xp), _ptr(pre), _ptr(y), N, n, d, _stream(stream)), "mhc_hc_pre")
+    return y
+
+
+def step_occupancy(d: int, flags: int = 0, n: int = N_STREAMS):
+    """(split, clusters resident at once) of the fused step on the current device."""
+    sp, cl = _I(0), _I(0)
+    _check(lib.mhc_step_occupancy(n, d, flags, ctypes.byref(sp), ctypes.byref(cl)),
+           "mhc_step_occupancy")
+    return sp.value, cl.value
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream; MHC_OK or MHC_ERR_TIMEOUT (then cleared)."""
+    return int(lib.mhc_get_status(_stream(stream)))

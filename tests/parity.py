@@ -1,0 +1,75 @@
+"""Comparison rules for the CUDA path against the CPU oracle.
+
+Tolerances (stated once, used by every GPU test):
+  * X' and y_hat: bit-exact. Both sides evaluate the same float32 operations in the same order
+    before the bf16 rounding, so the rounding decision is identical.
+  * y: within 2 bf16 ulps of the oracle (the RMS statistic is summed in a different order).
+  * p, u, C: absolute error <= 1e-5.
+  * m (the 24 mix numbers): per token, max |dm| <= 1e-4 * max |m|.
+"""
+import numpy as np
+
+import oracle as O
+
+TOL_PUC = 1e-5
+TOL_M_REL = 1e-4
+Y_ULPS = 2
+
+
+def to64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def bf16_ulp(ref):
+    a = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.frexp(a)[1]
+    return np.maximum(np.ldexp(1.0, e - 8), 2.0 ** -133)
+
+
+def assert_bf16_within(got, ref, ulps=Y_ULPS, name="y"):
+    got = np.asarray(got, dtype=np.float64)
+    diff = np.abs(got - ref)
+    lim = ulps * bf16_ulp(ref)
+    bad = diff > lim
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} beyond {ulps} bf16 ulps; "
+                             f"first at {idx.tolist()}: got {got[tuple(idx[0])]}, "
+                             f"want {ref[tuple(idx[0])]}")
+
+
+def assert_exact(got, ref, name):
+    got = np.asarray(got, dtype=np.float64)
+    neq = got != ref
+    if neq.any():
+        idx = np.argwhere(neq)[:5]
+        raise AssertionError(f"{name}: {int(neq.sum())} of {neq.size} differ; first at "
+                             f"{idx.tolist()}: got {got[tuple(idx[0])]}, want {ref[tuple(idx[0])]}")
+
+
+def assert_abs(got, ref, tol, name):
+    err = np.max(np.abs(np.asarray(got, dtype=np.float64) - ref)) if ref.size else 0.0
+    assert err <= tol, f"{name}: max abs error {err:.3e} > {tol:.1e}"
+
+
+def assert_mixes(got, ref, rel=TOL_M_REL):
+    got = np.asarray(got, dtype=np.float64)
+    scale = np.max(np.abs(ref), axis=1, keepdims=True)
+    err = np.max(np.abs(got - ref), axis=1, keepdims=True)
+    worst = float(np.max(err / scale)) if ref.size else 0.0
+    assert worst <= rel, f"mixes: worst per-token relative error {worst:.3e} > {rel:.1e}"
+
+
+def oracle_step(inp, **kw):
+    a = O.inputs_to_f64(inp)
+    return O.fused_step(a["X"], a["F"], a["pre"], a["post"], a["comb"], a["W"], a["scale"],
+                        a["base"], a["gain"], **kw)
+
+
+def check_step(out, ref, with_mixes=True):
+    assert_exact(to64(out["Xp"]), ref["Xp"], "X'")
+    assert_bf16_within(to64(out["y"]), ref["y"])
+    for k in ("pre", "post", "comb"):
+        assert_abs(to64(out[k]), ref[k], TOL_PUC, k)
+    if with_mixes:
+        assert_mixes(to64(out["mixes"]), ref["mixes"])

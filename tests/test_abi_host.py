@@ -1,0 +1,119 @@
+"""The C-ABI library on the host: it loads, exports every call include/mhc.h declares, and its
+argument validation rejects bad calls before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mhc.h")
+
+
+@pytest.fixture(scope="module")
+def M():
+    from stream_residual_fusion_gb300 import build
+    build.build()
+    import stream_residual_fusion_gb300.mhc as m
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mhc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(M):
+    names = _declared()
+    assert "mhc_fused_step" in names and "mhc_rmsnorm" in names
+    lib = ctypes.CDLL(M.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+        assert name in M.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_status_codes_match_header(M):
+    text = open(HEADER).read()
+    codes = dict((k, int(v)) for k, v in re.findall(r"#define (MHC_[A-Z_]+)\s+(-?\d+)\b", text))
+    for k, v in codes.items():
+        if hasattr(M, k):
+            assert getattr(M, k) == v
+    for code in range(-7, 1):
+        assert M.lib.mhc_strerror(code)
+    assert M.lib.mhc_strerror(-99) == b"unknown status code"
+
+
+def test_sizes(M):
+    assert M.lib.mhc_packed_weights_bytes(4, 5120) == 3 * 24 * 20480 * 2
+    assert M.lib.mhc_workspace_bytes(4, 5120) >= M.lib.mhc_packed_weights_bytes(4, 5120)
+    assert M.lib.mhc_packed_weights_bytes(3, 5120) == 0
+
+
+# Fake device addresses: validation runs before any CUDA call, so these are never dereferenced.
+A = 1 << 32
+
+
+def _addr(i):
+    return ctypes.c_void_p(A + i * (1 << 28))
+
+
+def _fused(M, N=256, n=4, d=5120, iters=20, flags=0, ptrs=None, ws=None, ws_bytes=None):
+    p = [_addr(i) for i in range(15)] if ptrs is None else ptrs
+    ws = _addr(20) if ws is None else ws
+    wsb = M.lib.mhc_workspace_bytes(4, 5120) if ws_bytes is None else ws_bytes
+    return M.lib.mhc_fused_step(*p, N, n, d, iters, 1e-6, 1e-6, flags, ws, wsb, None)
+
+
+def test_fused_validation(M):
+    assert _fused(M, n=3) == M.MHC_ERR_SHAPE
+    assert _fused(M, N=-1) == M.MHC_ERR_SHAPE
+    assert _fused(M, iters=0) == M.MHC_ERR_SHAPE
+    assert _fused(M, d=5000) == M.MHC_ERR_SHAPE          # not a multiple of the tile width
+    assert _fused(M, d=8192) == M.MHC_ERR_SHAPE          # slice too wide for TMEM at split 8
+    assert _fused(M, flags=3 << 8) == M.MHC_ERR_SHAPE    # split 3 is not offered
+    assert _fused(M, flags=1 << 8) == M.MHC_ERR_SHAPE    # 5120 columns do not fit one CTA
+    p = [_addr(i) for i in range(15)]
+    p[0] = ctypes.c_void_p(A + 8)
+    assert _fused(M, ptrs=p) == M.MHC_ERR_ALIGN
+    p = [_addr(i) for i in range(15)]
+    p[1] = None
+    assert _fused(M, ptrs=p) == M.MHC_ERR_NULL
+    assert _fused(M, ws=ctypes.c_void_p(0)) == M.MHC_ERR_WORKSPACE
+    assert _fused(M, ws_bytes=100) == M.MHC_ERR_WORKSPACE
+    p = [_addr(i) for i in range(15)]
+    p[10] = ctypes.c_void_p(p[1].value + 4096)          # y_out inside F
+    assert _fused(M, ptrs=p) == M.MHC_ERR_ALIAS
+    p = [_addr(i) for i in range(15)]
+    p[9] = p[0]                                          # X_out == X: in place is allowed
+    assert _fused(M, N=0, ptrs=p) == M.MHC_OK
+    p = [_addr(i) for i in range(15)]
+    p[9] = ctypes.c_void_p(p[0].value + 16)              # partial overlap is not
+    assert _fused(M, ptrs=p) == M.MHC_ERR_ALIAS
+    assert _fused(M, ws=p[3]) == M.MHC_ERR_ALIAS         # workspace over an input
+    assert _fused(M, N=0) == M.MHC_OK                    # nothing to do, nothing launched
+
+
+def test_split_choices(M):
+    ok = {256: M.MHC_OK, 512: M.MHC_OK, 768: M.MHC_OK, 1024: M.MHC_OK, 2048: M.MHC_OK,
+          5120: M.MHC_OK, 6144: M.MHC_OK, 96: M.MHC_OK, 100: M.MHC_ERR_SHAPE, 7168: M.MHC_ERR_SHAPE}
+    for d, want in ok.items():
+        assert _fused(M, N=0, d=d, ws_bytes=1 << 40) == want, d
+
+
+def test_other_calls_validation(M):
+    p = [_addr(i) for i in range(8)]
+    lib = M.lib
+    assert lib.mhc_sinkhorn(*p[:6], 10, 4, 0, 1e-6, None) == M.MHC_ERR_SHAPE
+    assert lib.mhc_sinkhorn(*p[:6], 0, 4, 20, 1e-6, None) == M.MHC_OK
+    assert lib.mhc_sinkhorn(None, *p[1:6], 10, 4, 20, 1e-6, None) == M.MHC_ERR_NULL
+    assert lib.mhc_sinkhorn(None, *p[1:6], 0, 4, 20, 1e-6, None) == M.MHC_OK  # empty: no address needed
+    assert lib.mhc_rmsnorm(*p[:3], 10, 100, 1e-6, None) == M.MHC_ERR_SHAPE
+    assert lib.mhc_rmsnorm(p[0], p[1], p[0], 0, 128, 1e-6, None) == M.MHC_OK   # in place
+    q = [ctypes.c_void_p(A + 4), p[1], p[2]]
+    assert lib.mhc_rmsnorm(*q, 10, 128, 1e-6, None) == M.MHC_ERR_ALIGN
+    assert lib.mhc_hc_post(*p[:5], 10, 2, 128, 0, None) == M.MHC_ERR_SHAPE
+    assert lib.mhc_hc_pre(p[0], p[1], ctypes.c_void_p(p[0].value + 32), 10, 4, 128, None) == M.MHC_ERR_ALIAS
+    assert lib.mhc_pack_weights(p[0], ctypes.c_void_p(p[0].value + 64), 4, 128, None) == M.MHC_ERR_ALIAS
+    assert lib.mhc_mixes(*p[:8], 10, 4, 5120, 20, 1e-6, 1e-6, 0, None, 0, None) == M.MHC_ERR_WORKSPACE
+    assert lib.mhc_mixes(*p[:8], 0, 4, 5120, 20, 1e-6, 1e-6, 0, p[7], 1 << 30, None) == M.MHC_OK

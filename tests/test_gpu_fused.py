@@ -1,0 +1,181 @@
+"""Parity of the fused single-pass mHC step (mhc_fused_step / mhc_fused_step_packed) with the
+CPU oracle: several tiles with a ragged tail, every width split, both readings of comb, in place,
+edge cases, the bounded-wait status path, and the benchmark workloads (in full where the oracle
+finishes in seconds, else on sampled tokens plus properties that hold at any size)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.parity import (TOL_PUC, assert_abs, assert_bf16_within, assert_exact, check_step,
+                          oracle_step, to64)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def M():
+    from stream_residual_fusion_gb300 import build
+    build.build()
+    import stream_residual_fusion_gb300.mhc as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def synth():
+    from stream_residual_fusion_gb300 import synth as s
+    return s
+
+
+def _run(M, inp, **kw):
+    return M.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], inp["W"],
+                        inp["scale"], inp["base"], inp["gain"], with_mixes=True, **kw)
+
+
+CASES = [
+    # N, d, split (0 = automatic)
+    (1, 256, 0),
+    (128, 256, 1),
+    (200, 256, 1),
+    (300, 512, 2),
+    (300, 1024, 4),
+    (260, 2048, 8),
+    (300, 5120, 0),
+    (130, 6144, 8),
+]
+
+
+@pytest.mark.parametrize("N,d,split", CASES)
+def test_fused_parity(M, synth, N, d, split):
+    inp = synth.make_inputs(N, 4, d, seed=1000 + N + d, device=DEV, scale_uniform=True,
+                            x_stream_std=True)
+    out = _run(M, inp, flags=M.split_flag(split))
+    assert M.get_status() == M.MHC_OK
+    check_step(out, oracle_step(inp))
+
+
+def test_fused_comb_row_dest(M, synth):
+    inp = synth.make_inputs(150, 4, 1024, seed=5, device=DEV)
+    comb = torch.rand(150, 4, 4, device=DEV)            # not symmetric: the readings differ
+    inp["comb"] = comb
+    out = _run(M, inp, flags=M.COMB_ROW_DEST)
+    ref = oracle_step(inp, comb_row_dest=True)
+    check_step(out, ref)
+    other = oracle_step(inp, comb_row_dest=False)
+    assert np.any(other["Xp"] != ref["Xp"])
+
+
+def test_fused_packed_and_in_place(M, synth):
+    inp = synth.make_inputs(257, 4, 5120, seed=9, device=DEV, scale_uniform=True)
+    ref = oracle_step(inp)
+    Wp = M.pack_weights(inp["W"])
+    X = inp["X"].clone()
+    out = M.fused_step(X, inp["F"], inp["pre"], inp["post"], inp["comb"], None, inp["scale"],
+                       inp["base"], inp["gain"], with_mixes=True, W_packed=Wp,
+                       out={"Xp": X})
+    assert out["Xp"].data_ptr() == X.data_ptr()
+    check_step(out, ref)
+
+
+def test_fused_identity_tuple(M, synth):
+    """u_prev = 0 and C_prev = I leave the streams bit-identical; one-hot p_prev makes y the
+    RMSNorm of one stream."""
+    N, d = 140, 512
+    inp = synth.make_inputs(N, 4, d, seed=11, device=DEV)
+    inp["post"] = torch.zeros(N, 4, device=DEV)
+    inp["comb"] = torch.eye(4, device=DEV).expand(N, 4, 4).contiguous()
+    inp["pre"] = torch.tensor([0.0, 0.0, 1.0, 0.0], device=DEV).expand(N, 4).contiguous()
+    inp["gain"] = torch.rand(d, device=DEV) + 0.5
+    out = _run(M, inp)
+    assert torch.equal(out["Xp"], inp["X"])
+    assert_bf16_within(to64(out["y"]), O.rmsnorm(to64(inp["X"][:, 2]), to64(inp["gain"]), 1e-6))
+
+
+def test_fused_zero_tokens(M, synth):
+    inp = synth.make_inputs(0, 4, 5120, seed=1, device=DEV)
+    out = _run(M, inp)
+    assert out["Xp"].numel() == 0 and M.get_status() == M.MHC_OK
+
+
+def test_fused_tiny_eps_and_outliers(M, synth):
+    """norm_eps = 1e-20 (the formula block's value) and tokens scaled by 100."""
+    inp = synth.make_inputs(200, 4, 1024, seed=13, device=DEV, outlier_frac=0.05)
+    out = _run(M, inp, norm_eps=1e-20, hc_eps=1e-6)
+    check_step(out, oracle_step(inp, norm_eps=1e-20))
+
+
+def test_fused_sinkhorn_iterations(M, synth):
+    inp = synth.make_inputs(100, 4, 512, seed=17, device=DEV)
+    for iters in (1, 2, 7):
+        out = _run(M, inp, iters=iters)
+        check_step(out, oracle_step(inp, iters=iters))
+
+
+def test_bounded_wait_reports_timeout(M, synth):
+    """A wait that nothing completes gives up after ~2 ms, the call still finishes with correct
+    results, mhc_get_status reports the timeout once, and the next call is clean."""
+    inp = synth.make_inputs(130, 4, 512, seed=19, device=DEV)
+    out = _run(M, inp, flags=M.DEBUG_NEVER_ARRIVE)
+    assert M.get_status() == M.MHC_ERR_TIMEOUT
+    check_step(out, oracle_step(inp))
+    assert M.get_status() == M.MHC_OK
+    out = _run(M, inp)
+    assert M.get_status() == M.MHC_OK
+    check_step(out, oracle_step(inp))
+
+
+def test_unfused_chain_matches(M, synth):
+    """hc_post, hc_mixes, hc_pre and RMSNorm as four kernels give the fused step's results."""
+    inp = synth.make_inputs(300, 4, 5120, seed=23, device=DEV, scale_uniform=True)
+    fused = _run(M, inp)
+    Xp = M.hc_post(inp["X"], inp["F"], inp["post"], inp["comb"])
+    mx = M.mixes(Xp, inp["W"], inp["scale"], inp["base"])
+    y = M.rmsnorm(M.hc_pre(Xp, inp["pre"]), inp["gain"], 1e-6)
+    assert torch.equal(Xp, fused["Xp"])
+    for k in ("pre", "post", "comb"):
+        assert_abs(to64(mx[k]), to64(fused[k]), 1e-6, k)
+    assert_bf16_within(to64(y), to64(fused["y"]), 1, "y")
+
+
+# ---------------------------------------------------------------------------------------------
+# the benchmark workloads
+
+
+def _sample(N, outliers=None, k=384, seed=0):
+    rng = np.random.default_rng(seed)
+    picks = set(range(min(N, 130))) | set(range(max(0, N - 130), N))
+    picks |= set(rng.choice(N, size=min(N, k), replace=False).tolist())
+    if outliers is not None:
+        picks |= set(outliers.tolist())
+    return torch.tensor(sorted(picks), dtype=torch.long)
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill4k", "decode256"])
+def test_workload_full(M, synth, name):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_workload(w, seed=1)
+    inp = {k: v.to(DEV) for k, v in inp.items()}
+    out = _run(M, inp)
+    assert M.get_status() == M.MHC_OK
+    check_step(out, oracle_step(inp))
+
+
+@pytest.mark.parametrize("name", ["prefill32k", "prefill128k"])
+def test_workload_sampled(M, synth, name):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_workload(w, seed=1, device=DEV)
+    out = _run(M, inp)
+    assert M.get_status() == M.MHC_OK
+    # properties that hold for every token
+    for k in ("Xp", "y", "pre", "post", "comb", "mixes"):
+        assert torch.isfinite(out[k].float()).all(), k
+    col = out["comb"].sum(dim=1)
+    assert (col <= 1.0 + 1e-5).all() and (out["comb"] > 0).all()
+    assert ((out["post"] > 0) & (out["post"] < 2)).all()
+    # sampled tokens against the oracle, every outlier token included
+    idx = _sample(w.N, inp.get("outliers", None) if "outliers" in inp else None)
+    sub = synth.subset({k: v for k, v in inp.items()}, idx.to(DEV))
+    ref = oracle_step(sub)
+    got = {k: v[idx.to(DEV)] for k, v in out.items()}
+    check_step(got, ref)

@@ -1,0 +1,101 @@
+"""Parity of the standalone kernels (split + Sinkhorn, RMSNorm, hc_post, hc_pre, weight packing,
+hc_mixes) against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.parity import TOL_PUC, assert_abs, assert_bf16_within, assert_exact, assert_mixes, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    from stream_residual_fusion_gb300 import build
+    build.build()
+    import stream_residual_fusion_gb300.mhc as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def synth():
+    from stream_residual_fusion_gb300 import synth as s
+    return s
+
+
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("N,std,iters", [(1, 1.0, 20), (1000, 3.0, 20), (257, 8.0, 20),
+                                         (64, 2.0, 1), (64, 2.0, 3)])
+def test_sinkhorn(M, N, std, iters):
+    g = torch.Generator(device=DEV).manual_seed(N)
+    mixes = torch.randn(N, 24, generator=g, device=DEV) * std
+    scale = torch.tensor([0.7, 1.3, 1.9], device=DEV)
+    base = torch.randn(24, generator=g, device=DEV)
+    o = M.sinkhorn(mixes, scale, base, iters=iters, hc_eps=1e-6)
+    p, u, L = O.hc_split(to64(mixes), to64(scale), to64(base), 4, 1e-6)
+    C = O.sinkhorn(L, iters, 1e-6)
+    assert_abs(to64(o["pre"]), p, TOL_PUC, "pre")
+    assert_abs(to64(o["post"]), u, TOL_PUC, "post")
+    assert_abs(to64(o["comb"]), C, TOL_PUC, "comb")
+
+
+def test_sinkhorn_equal_logits_closed_form(M):
+    mixes = torch.zeros(5, 24, device=DEV)
+    o = M.sinkhorn(mixes, torch.ones(3, device=DEV), torch.zeros(24, device=DEV), iters=20)
+    C = O.sinkhorn(np.zeros((5, 4, 4)), 20, 1e-6)
+    assert_abs(to64(o["comb"]), C, 1e-6, "comb")
+    assert_abs(to64(o["pre"]), np.full((5, 4), 0.5 + 1e-6), 1e-7, "pre")
+    assert_abs(to64(o["post"]), np.ones((5, 4)), 1e-7, "post")
+
+
+@pytest.mark.parametrize("N,d,eps", [(1, 128, 1e-6), (333, 5120, 1e-6), (64, 1024, 1e-20)])
+def test_rmsnorm(M, N, d, eps):
+    g = torch.Generator(device=DEV).manual_seed(d)
+    x = (torch.randn(N, d, generator=g, device=DEV) * 3).to(torch.bfloat16)
+    gain = torch.rand(d, generator=g, device=DEV) + 0.5
+    y = M.rmsnorm(x, gain, eps)
+    assert_bf16_within(to64(y), O.rmsnorm(to64(x), to64(gain), eps))
+
+
+def test_rmsnorm_zero_row_tiny_eps(M):
+    x = torch.zeros(3, 256, dtype=torch.bfloat16, device=DEV)
+    y = M.rmsnorm(x, torch.ones(256, device=DEV), 1e-20)
+    assert torch.count_nonzero(y).item() == 0 and torch.isfinite(y.float()).all()
+
+
+@pytest.mark.parametrize("row_dest", [False, True])
+def test_hc_post_and_pre_bit_exact(M, synth, row_dest):
+    inp = synth.make_inputs(77, 4, 768, seed=3, device=DEV)
+    Xp = M.hc_post(inp["X"], inp["F"], inp["post"], inp["comb"],
+                   flags=M.COMB_ROW_DEST if row_dest else 0)
+    a = O.inputs_to_f64(inp)
+    ref = O.hc_post(a["X"], a["F"], a["post"], a["comb"], comb_row_dest=row_dest)
+    assert_exact(to64(Xp), ref, "X'")
+    yh = M.hc_pre(Xp, inp["pre"])
+    assert_exact(to64(yh), O.hc_pre(ref, a["pre"]), "y_hat")
+
+
+def test_pack_weights_reconstructs(M):
+    g = torch.Generator(device=DEV).manual_seed(0)
+    W = torch.randn(24, 4 * 512, generator=g, device=DEV) * 0.02
+    W[0, :8] = torch.tensor([1e-30, -1e-30, 3.0e38, 0.0, -0.0, 1.0, 2.0 ** -126, 1e-40], device=DEV)
+    P = M.pack_weights(W).double().cpu().numpy()
+    recon = (P[48:72] + P[24:48]) + P[0:24]
+    w = W.double().cpu().numpy()
+    assert np.array_equal(P[0:24], O.bf16_round(w))           # the hi plane is bf16(W)
+    np.testing.assert_allclose(recon, w, rtol=2.0 ** -23, atol=1e-44)
+
+
+@pytest.mark.parametrize("N,d,split", [(1, 256, 0), (200, 512, 2), (300, 5120, 0), (129, 1024, 4)])
+def test_mixes(M, synth, N, d, split):
+    inp = synth.make_inputs(N, 4, d, seed=N + d, device=DEV, scale_uniform=True)
+    o = M.mixes(inp["X"], inp["W"], inp["scale"], inp["base"], flags=M.split_flag(split))
+    a = O.inputs_to_f64(inp)
+    m, p, u, C = O.hc_mixes(a["X"], a["W"], a["scale"], a["base"], 20, 1e-6, 1e-6)
+    assert_mixes(to64(o["mixes"]), m)
+    assert_abs(to64(o["pre"]), p, TOL_PUC, "pre")
+    assert_abs(to64(o["post"]), u, TOL_PUC, "post")
+    assert_abs(to64(o["comb"]), C, TOL_PUC, "comb")

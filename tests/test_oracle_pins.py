@@ -61,6 +61,47 @@ def test_bf16_matches_independent_conversion_from_float32():
     assert np.array_equal(got, ref)
 
 
+def _round_f32_exact(fr):
+    """Nearest float32 to the rational fr, ties to even (by exact comparison)."""
+    r = np.float32(float(fr))
+    cands = {float(r), float(np.nextafter(r, np.float32(np.inf))), float(np.nextafter(r, np.float32(-np.inf)))}
+    best = sorted(cands, key=lambda v: (abs(Fraction(v) - fr),
+                                        int(np.float32(v).view(np.uint32)) & 1))
+    return np.float32(best[0])
+
+
+def test_fma32_against_exact_rationals():
+    """Random float32 triples over a range of exponent gaps, and near-tie triples whose product
+    has few bits: fma32 must equal a*b + c rounded once (exact rationals, ties to even)."""
+    rng = np.random.default_rng(21)
+    trips = []
+    for gap in (0, 8, 24, 30, 40):
+        a = rng.standard_normal(400).astype(np.float32)
+        b = rng.standard_normal(400).astype(np.float32)
+        c = (rng.standard_normal(400) * 2.0 ** gap).astype(np.float32)
+        trips += list(zip(a, b, c))
+    a = (rng.integers(1, 256, 2000) * 2.0 ** -7).astype(np.float32)    # 8-bit values
+    b = (rng.integers(1, 256, 2000) * 2.0 ** -9).astype(np.float32)
+    c = (rng.integers(-2 ** 20, 2 ** 20, 2000) * 2.0 ** -12).astype(np.float32)
+    trips += list(zip(a, b, c))
+    A, B, Cc = (np.array(v, dtype=np.float32) for v in zip(*trips))
+    got = O.fma32(A, B, Cc)
+    for x, y, z, g in zip(A, B, Cc, got):
+        want = _round_f32_exact(Fraction(float(x)) * Fraction(float(y)) + Fraction(float(z)))
+        assert g == want, (x, y, z, g, want)
+
+
+def test_fma32_tie_broken_by_lost_bits():
+    """a*b + c = (2^40 + 2^17 + 2^16) - 2^-30: the float64 sum lands exactly on the float32 tie
+    and rounding it again would go to even (2^40 + 2^18); the exact value is below the tie."""
+    a = np.float32(2.0 ** 8 * (1 + 2.0 ** -23))
+    b = np.float32(2.0 ** 8 * (1 - 2.0 ** -23))
+    c = np.float32(2.0 ** 40 + 2.0 ** 17)
+    assert np.float32(np.float64(a) * np.float64(b) + np.float64(c)) == np.float32(2.0 ** 40 + 2.0 ** 18)
+    assert O.fma32(a, b, c) == np.float32(2.0 ** 40 + 2.0 ** 17)
+    assert O.fma32(-a, b, -c) == -np.float32(2.0 ** 40 + 2.0 ** 17)
+
+
 # ---------------------------------------------------------------------------------------------
 # plain Sinkhorn: the page's worked example
 
