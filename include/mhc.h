@@ -83,7 +83,7 @@ size_t mhc_workspace_bytes(int n, int d);
  *   X_out     bf16 [N, n, d]      may equal X (in place); no other overlap
  *   y_out     bf16 [N, d]
  *   pre_out, post_out fp32 [N, n]; comb_out fp32 [N, n, n]; mixes_out fp32 [N, (2+n)n] or NULL
- *   d: multiple of 32*split and d/split <= 768 for the chosen split (d = 5120 uses split 8).
+ *   d: multiple of 16*split and d/split <= 704 for the chosen split (d = 5120 uses split 8).
  *   workspace: >= mhc_workspace_bytes(n, d) device bytes; W_mix is packed into it each call.
  * Returns MHC_OK or a negative code. N == 0 returns MHC_OK once the shape is valid, without
  * looking at the pointers (empty tensors may have none) and without launching.               */
@@ -137,8 +137,9 @@ int mhc_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int n, 
 
 /* ---- weights packing -----------------------------------------------------------------------
  * Split fp32 W_mix [(2+n)n, n*d] into three bf16 planes hi + mid + lo (each the bf16 rounding
- * of what the previous planes left), stored as packed [3*(2+n)n, n*d]: rows 0..23 hi,
- * 24..47 mid, 48..71 lo. The three planes carry W to float32 accuracy for the tensor cores.   */
+ * of what the previous planes left), stored as packed [3*(2+n)n, n*d]: plane pl (0 hi, 1 mid,
+ * 2 lo) of mix row r is packed row 36*(r/12) + 12*pl + r%12. The three planes carry W to
+ * float32 accuracy for the tensor cores.                                                     */
 int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* stream);
 
 /* ---- status --------------------------------------------------------------------------------
@@ -150,6 +151,14 @@ int mhc_get_status(void* stream);
  * flags) and how many such clusters the device can hold at once (cudaOccupancyMaxActiveClusters).
  * Diagnostic only; needs a GPU.                                                               */
 int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters);
+/* Phase tracing of the fused step (off by default). With a device buffer set, every later
+ * launch whose grid fits records, per CTA, 8 uint64 values from the GPU's nanosecond timer:
+ * the start time, then nanoseconds since the start at: loads issued, main loop done, partials
+ * ready, cluster reduced, mix numbers written, y written, end (slot 7 carries the SM id in bits
+ * 40 and up). CTA index = tile * split + rank in the cluster. Launches
+ * with more CTAs than the buffer holds record nothing. NULL turns tracing off. The buffer stays
+ * caller-owned; it must outlive the launches that write it. Not thread-safe.                  */
+int mhc_set_trace(void* buffer, int64_t bytes);
 /* Static text for a status code.                                                              */
 const char* mhc_strerror(int code);
 /* Library ABI version (major*100 + minor).                                                    */

@@ -17,6 +17,8 @@ __device__ unsigned g_status;
 constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
+unsigned long long* g_trace = nullptr;
+int64_t g_trace_ctas = 0;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -59,6 +61,10 @@ unsigned* status_word() {
     g_status_ptr[dev] = static_cast<unsigned*>(p);
   }
   return g_status_ptr[dev];
+}
+
+unsigned long long* trace_buffer(int64_t ctas) {
+  return (g_trace != nullptr && ctas <= g_trace_ctas) ? g_trace : nullptr;
 }
 
 }  // namespace mhc
@@ -324,6 +330,13 @@ int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters) 
   if (rc != MHC_OK) return rc;
   *split = sp;
   return cuda_code(step_occupancy(sp, clusters));
+}
+
+int mhc_set_trace(void* buffer, int64_t bytes) {
+  if (buffer != nullptr && (!aligned16(buffer) || bytes < 64)) return MHC_ERR_ALIGN;
+  g_trace = static_cast<unsigned long long*>(buffer);
+  g_trace_ctas = buffer == nullptr ? 0 : bytes / 64;
+  return MHC_OK;
 }
 
 int mhc_version(void) { return 100; }

@@ -7,6 +7,8 @@ namespace mhc {
 
 // Device address of the library's status word on the current device (see mhc_get_status).
 unsigned* status_word();
+// The trace buffer set by mhc_set_trace if it holds `ctas` CTAs' records, else nullptr.
+unsigned long long* trace_buffer(int64_t ctas);
 
 constexpr unsigned STATUS_TIMEOUT = 1u;
 

@@ -6,11 +6,19 @@
 //   L_jk = s_2 m_{8+4j+k} + b_{8+4j+k}
 //   C    = softmax over k (max subtracted) + eps; columns / (sum + eps);
 //          then (iters-1) x [rows / (sum + eps), columns / (sum + eps)].
-// One thread owns one token. Divisions by a row or column sum are a correctly rounded
-// reciprocal followed by a multiply (4 reciprocals instead of 16 divisions per step).
+// split_sinkhorn: one thread owns one token. split_sinkhorn_row: four lanes own one token, lane j
+// holding row j of comb; column sums go through warp shuffles. Divisions by a row or column sum
+// are a reciprocal followed by a multiply (4 reciprocals instead of 16 divisions per step).
 #pragma once
 
 namespace mhc {
+
+// Hardware reciprocal (rcp.approx: within 1 ulp for normal positive inputs).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 __device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 
@@ -61,6 +69,42 @@ __device__ __forceinline__ void split_sinkhorn(const float (&m)[24], float s0, f
   col_step();
   for (int it = 1; it < iters; ++it) {
     row_step();
+    col_step();
+  }
+}
+
+// Four cooperating lanes (lane j of the aligned group of 4 holds row j). Inputs: this row's
+// four logit mix numbers mrow[k] = m[8+4j+k], and m[j], m[4+j]. Outputs: p_j, u_j, comb row j.
+// All four lanes must call it together (shuffles over the group).
+__device__ __forceinline__ void split_sinkhorn_row(const float (&mrow)[4], float m_p, float m_u,
+                                                   int j, float s0, float s1, float s2,
+                                                   const float* __restrict__ base, int iters,
+                                                   float eps, float& p, float& u, float (&c)[4]) {
+  p = sigmoid_f(fmaf(m_p, s0, __ldg(base + j))) + eps;
+  u = 2.0f * sigmoid_f(fmaf(m_u, s1, __ldg(base + 4 + j)));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) c[k] = fmaf(mrow[k], s2, __ldg(base + 8 + 4 * j + k));
+  {
+    const float mx = fmaxf(fmaxf(c[0], c[1]), fmaxf(c[2], c[3]));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = expf(c[k] - mx);
+    const float r = rcp_approx((c[0] + c[1]) + (c[2] + c[3]));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] = fmaf(c[k], r, eps);
+  }
+  auto col_step = [&]() {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float t = c[k] + __shfl_xor_sync(0xffffffffu, c[k], 1);
+      t += __shfl_xor_sync(0xffffffffu, t, 2);
+      c[k] *= rcp_approx(t + eps);
+    }
+  };
+  col_step();
+  for (int it = 1; it < iters; ++it) {
+    const float r = rcp_approx(((c[0] + c[1]) + (c[2] + c[3])) + eps);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c[k] *= r;
     col_step();
   }
 }

@@ -9,8 +9,9 @@
 namespace mhc {
 namespace {
 
-// W fp32 [24, K] -> bf16 [72, K]: rows r, 24+r, 48+r hold hi, mid, lo with
-// hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid). The differences are exact in fp32.
+// W fp32 [24, K] -> bf16 [72, K]: hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid)
+// (the differences are exact in fp32). Plane pl of mix row r goes to packed row
+// 36*(r/12) + 12*pl + r%12: each half of the 24 mix rows keeps its three planes together.
 __global__ void pack_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ P, int64_t K) {
   const int64_t total = 24 * K;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -22,9 +23,10 @@ __global__ void pack_kernel(const float* __restrict__ W, __nv_bfloat16* __restri
     const __nv_bfloat16 mid = __float2bfloat16_rn(rem1);
     const float rem2 = rem1 - __bfloat162float(mid);
     const __nv_bfloat16 lo = __float2bfloat16_rn(rem2);
-    P[r * K + col] = hi;
-    P[(24 + r) * K + col] = mid;
-    P[(48 + r) * K + col] = lo;
+    const int64_t base_row = 36 * (r / 12) + r % 12;
+    P[base_row * K + col] = hi;
+    P[(base_row + 12) * K + col] = mid;
+    P[(base_row + 24) * K + col] = lo;
   }
 }
 

@@ -62,6 +62,7 @@ SIGNATURES = {
     "mhc_pack_weights": (_I, [_P, _P, _I, _I, _P]),
     "mhc_get_status": (_I, [_P]),
     "mhc_strerror": (ctypes.c_char_p, [_I]),
+    "mhc_set_trace": (_I, [_P, _I64]),
     "mhc_step_occupancy": (_I, [_I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "mhc_version": (_I, []),
 }
@@ -253,6 +254,16 @@ def step_occupancy(d: int, flags: int = 0, n: int = N_STREAMS):
     _check(lib.mhc_step_occupancy(n, d, flags, ctypes.byref(sp), ctypes.byref(cl)),
            "mhc_step_occupancy")
     return sp.value, cl.value
+
+
+def set_trace(buffer=None):
+    """Record per-CTA phase timestamps of later fused launches into `buffer` (a CUDA int64
+    tensor of 8 entries per CTA), or turn tracing off with None."""
+    if buffer is None:
+        _check(lib.mhc_set_trace(None, 0), "mhc_set_trace")
+    else:
+        _check(lib.mhc_set_trace(_ptr(buffer), buffer.numel() * buffer.element_size()),
+               "mhc_set_trace")
 
 
 def get_status(stream=None) -> int:

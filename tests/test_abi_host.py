@@ -69,7 +69,7 @@ def test_fused_validation(M):
     assert _fused(M, n=3) == M.MHC_ERR_SHAPE
     assert _fused(M, N=-1) == M.MHC_ERR_SHAPE
     assert _fused(M, iters=0) == M.MHC_ERR_SHAPE
-    assert _fused(M, d=5000) == M.MHC_ERR_SHAPE          # not a multiple of the tile width
+    assert _fused(M, d=5000) == M.MHC_ERR_SHAPE          # not a multiple of the tile width (16*8)
     assert _fused(M, d=8192) == M.MHC_ERR_SHAPE          # slice too wide for TMEM at split 8
     assert _fused(M, flags=3 << 8) == M.MHC_ERR_SHAPE    # split 3 is not offered
     assert _fused(M, flags=1 << 8) == M.MHC_ERR_SHAPE    # 5120 columns do not fit one CTA
@@ -95,8 +95,9 @@ def test_fused_validation(M):
 
 
 def test_split_choices(M):
-    ok = {256: M.MHC_OK, 512: M.MHC_OK, 768: M.MHC_OK, 1024: M.MHC_OK, 2048: M.MHC_OK,
-          5120: M.MHC_OK, 6144: M.MHC_OK, 96: M.MHC_OK, 100: M.MHC_ERR_SHAPE, 7168: M.MHC_ERR_SHAPE}
+    ok = {256: M.MHC_OK, 512: M.MHC_OK, 704: M.MHC_OK, 1024: M.MHC_OK, 2048: M.MHC_OK,
+          5120: M.MHC_OK, 5632: M.MHC_OK, 6144: M.MHC_ERR_SHAPE, 96: M.MHC_OK, 16: M.MHC_OK,
+          100: M.MHC_ERR_SHAPE, 7168: M.MHC_ERR_SHAPE}
     for d, want in ok.items():
         assert _fused(M, N=0, d=d, ws_bytes=1 << 40) == want, d
 

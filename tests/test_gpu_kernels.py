@@ -78,15 +78,23 @@ def test_hc_post_and_pre_bit_exact(M, synth, row_dest):
     assert_exact(to64(yh), O.hc_pre(ref, a["pre"]), "y_hat")
 
 
+def _planes(P):
+    """hi, mid, lo planes [24, K] from the packed layout (plane pl of row r at 36*(r//12)+12*pl+r%12)."""
+    rows = np.arange(24)
+    base = 36 * (rows // 12) + rows % 12
+    return P[base], P[base + 12], P[base + 24]
+
+
 def test_pack_weights_reconstructs(M):
     g = torch.Generator(device=DEV).manual_seed(0)
     W = torch.randn(24, 4 * 512, generator=g, device=DEV) * 0.02
     W[0, :8] = torch.tensor([1e-30, -1e-30, 3.0e38, 0.0, -0.0, 1.0, 2.0 ** -126, 1e-40], device=DEV)
-    P = M.pack_weights(W).double().cpu().numpy()
-    recon = (P[48:72] + P[24:48]) + P[0:24]
+    hi, mid, lo = _planes(M.pack_weights(W).double().cpu().numpy())
     w = W.double().cpu().numpy()
-    assert np.array_equal(P[0:24], O.bf16_round(w))           # the hi plane is bf16(W)
-    np.testing.assert_allclose(recon, w, rtol=2.0 ** -23, atol=1e-44)
+    assert np.array_equal(hi, O.bf16_round(w))                # the hi plane is bf16(W)
+    recon = (lo + mid) + hi
+    # three bf16 planes hold every float32 down to bf16's subnormal step 2^-133
+    np.testing.assert_allclose(recon, w, rtol=2.0 ** -23, atol=2.0 ** -133)
 
 
 @pytest.mark.parametrize("N,d,split", [(1, 256, 0), (200, 512, 2), (300, 5120, 0), (129, 1024, 4)])
