@@ -39,7 +39,7 @@ SMALL_BYTES_PER_TOKEN = 16 + 16 + 64 + 16 + 16 + 64  # p,u,C previous in; p,u,C 
 def algorithmic_bytes(N: int, d: int = 5120) -> int:
     """Bytes one fused launch must move: the streams and small per-token vectors, plus the packed
     weights and the gain once."""
-    return N * (STREAM_BYTES_PER_TOKEN + SMALL_BYTES_PER_TOKEN) + 72 * 4 * d * 2 + d * 4
+    return N * (STREAM_BYTES_PER_TOKEN + SMALL_BYTES_PER_TOKEN) + 640 * d + d * 4
 
 
 def measured_peaks():
@@ -52,7 +52,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("fused.cu", "ptx.cuh", "mix_math.cuh"):
+    for f in ("fused.cu", "ptx.cuh", "mix_math.cuh", "layout.cuh"):
         with open(os.path.join(ROOT, "stream_residual_fusion_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -244,7 +244,7 @@ def run_ours(args):
     out = {"Xp": torch.empty_like(inp["X"]), "y": torch.empty(N, d, dtype=torch.bfloat16, device=dev),
            "pre": torch.empty(N, 4, device=dev), "post": torch.empty(N, 4, device=dev),
            "comb": torch.empty(N, 4, 4, device=dev)}
-    Wp = torch.empty(3 * 24, 4 * d, dtype=torch.bfloat16, device=dev)
+    Wp = torch.empty(mhc.packed_weights_bytes(d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev_a=None, ev_b=None):

@@ -53,8 +53,11 @@ extern "C" {
 #define MHC_SPLIT_MASK           (0xFu << MHC_SPLIT_SHIFT)
 
 /* ---- sizes ------------------------------------------------------------------------------- */
-/* Bytes of the packed projection weights: 3 bf16 planes of W_mix, [3*(2+n)*n, n*d].           */
+/* Bytes of the packed projection weights (3 bf16 planes of W_mix plus padding, in the layout
+ * described at mhc_pack_weights). 0 if (n, d) cannot be packed.                             */
 size_t mhc_packed_weights_bytes(int n, int d);
+/* Columns of d per block of the packed weights (B below).                                    */
+int mhc_packed_block_columns(void);
 /* Workspace of mhc_fused_step / mhc_mixes (the packed weights).                              */
 size_t mhc_workspace_bytes(int n, int d);
 
@@ -83,7 +86,8 @@ size_t mhc_workspace_bytes(int n, int d);
  *   X_out     bf16 [N, n, d]      may equal X (in place); no other overlap
  *   y_out     bf16 [N, d]
  *   pre_out, post_out fp32 [N, n]; comb_out fp32 [N, n, n]; mixes_out fp32 [N, (2+n)n] or NULL
- *   d: multiple of 16*split and d/split <= 704 for the chosen split (d = 5120 uses split 8).
+ *   d: for the chosen split, d/split must be a multiple of 2B (B = mhc_packed_block_columns())
+ *      between 4B and 640 (d = 5120 uses split 8).
  *   workspace: >= mhc_workspace_bytes(n, d) device bytes; W_mix is packed into it each call.
  * Returns MHC_OK or a negative code. N == 0 returns MHC_OK once the shape is valid, without
  * looking at the pointers (empty tensors may have none) and without launching.               */
@@ -137,9 +141,13 @@ int mhc_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int n, 
 
 /* ---- weights packing -----------------------------------------------------------------------
  * Split fp32 W_mix [(2+n)n, n*d] into three bf16 planes hi + mid + lo (each the bf16 rounding
- * of what the previous planes left), stored as packed [3*(2+n)n, n*d]: plane pl (0 hi, 1 mid,
- * 2 lo) of mix row r is packed row 36*(r/12) + 12*pl + r%12. The three planes carry W to
- * float32 accuracy for the tensor cores.                                                     */
+ * of what the previous planes left); the three planes carry W to float32 accuracy for the
+ * tensor cores. The packed buffer is the fused kernel's shared-memory image, d/B blocks of B
+ * columns (B = mhc_packed_block_columns()): block b = [n streams][80 rows][B columns] bf16 of
+ * columns [b*B, (b+1)*B) of each stream; plane pl (0 hi, 1 mid, 2 lo) of mix row r is row
+ * 36*(r/12) + 12*pl + r%12, rows 72..79 are zero, and the 16-byte chunks of each row are
+ * swizzled: chunk c of row r is stored at chunk c ^ ((r*2B/128) mod (B/8)).
+ * d must be a multiple of B.                                                                 */
 int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* stream);
 
 /* ---- status --------------------------------------------------------------------------------

@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmhc.so")
 SOURCES = ["fused.cu", "small.cu", "abi.cu"]
-HEADERS = ["ptx.cuh", "mix_math.cuh", "internal.h"]
+HEADERS = ["ptx.cuh", "mix_math.cuh", "internal.h", "layout.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: a separate float32 multiply and add must stay two roundings (hc_post and hc_pre

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "layout.cuh"
 #include "mhc.h"
 
 namespace mhc {
@@ -112,7 +113,7 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
                        span(workspace, workspace ? ws_bytes : 0)};
   if (!aliasing_ok(outs, ins, 0, 0)) return MHC_ERR_ALIAS;
   if (!workspace) {  // pre-packed weights are an input too
-    const Span packed_in[] = {span(W_packed, 144 * K)};
+    const Span packed_in[] = {span(W_packed, mhc_packed_weights_bytes(4, d))};
     if (!aliasing_ok(outs, packed_in)) return MHC_ERR_ALIAS;
   }
 
@@ -152,18 +153,20 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
 extern "C" {
 
 size_t mhc_packed_weights_bytes(int n, int d) {
-  if (n != 4 || d <= 0) return 0;
-  return static_cast<size_t>(3) * (2 + n) * n * static_cast<size_t>(n) * d * 2;
+  if (n != 4 || d <= 0 || d % STEP_DC != 0) return 0;
+  return static_cast<size_t>(d / STEP_DC) * STEP_WBLOCK_BYTES;
 }
 
 size_t mhc_workspace_bytes(int n, int d) { return mhc_packed_weights_bytes(n, d); }
 
+int mhc_packed_block_columns(void) { return STEP_DC; }
+
 int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* stream) {
   if (!W_mix || !W_packed) return MHC_ERR_NULL;
-  if (n != 4 || d <= 0 || d % 8 != 0) return MHC_ERR_SHAPE;
+  if (n != 4 || d <= 0 || d % STEP_DC != 0) return MHC_ERR_SHAPE;
   if (!aligned16(W_mix) || !aligned16(W_packed)) return MHC_ERR_ALIGN;
   const uint64_t K = 4ull * d;
-  if (overlap(span(W_mix, 96 * K), span(W_packed, 144 * K))) return MHC_ERR_ALIAS;
+  if (overlap(span(W_mix, 96 * K), span(W_packed, mhc_packed_weights_bytes(4, d)))) return MHC_ERR_ALIAS;
   return cuda_code(launch_pack(W_mix, W_packed, d, static_cast<cudaStream_t>(stream)));
 }
 

@@ -52,6 +52,7 @@ _SZ = ctypes.c_size_t
 SIGNATURES = {
     "mhc_packed_weights_bytes": (_SZ, [_I, _I]),
     "mhc_workspace_bytes": (_SZ, [_I, _I]),
+    "mhc_packed_block_columns": (_I, []),
     "mhc_fused_step": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_fused_step_packed": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P]),
     "mhc_mixes": (_I, [_P] * 8 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
@@ -129,7 +130,7 @@ def pack_weights(W, out=None, stream=None):
     n = N_STREAMS
     d = W.shape[1] // n
     if out is None:
-        out = torch.empty(3 * MIX, n * d, dtype=torch.bfloat16, device=W.device)
+        out = torch.empty(packed_weights_bytes(d, n), dtype=torch.uint8, device=W.device)
     _check(lib.mhc_pack_weights(_ptr(W), _ptr(out), n, d, _stream(stream)), "mhc_pack_weights")
     return out
 
@@ -163,7 +164,7 @@ def fused_step(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, it
     common_out = [_ptr(o["Xp"]), _ptr(o["y"]), _ptr(o["pre"]), _ptr(o["post"]), _ptr(o["comb"]),
                   _ptr(o.get("mixes"))]
     if W_packed is not None:
-        _need(W_packed, torch.bfloat16, "W_packed")
+        _need(W_packed, torch.uint8, "W_packed")
         rc = lib.mhc_fused_step_packed(
             _ptr(X), _ptr(F), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev), _ptr(W_packed),
             _ptr(scale), _ptr(base), _ptr(gain), *common_out, N, n, d, iters, hc_eps, norm_eps,

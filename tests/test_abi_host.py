@@ -45,7 +45,11 @@ def test_status_codes_match_header(M):
 
 
 def test_sizes(M):
-    assert M.lib.mhc_packed_weights_bytes(4, 5120) == 3 * 24 * 20480 * 2
+    B = M.lib.mhc_packed_block_columns()
+    assert B in (16, 32, 64)
+    # d/B blocks x 4 streams x 80 rows (72 = 3 planes x 24 mix rows, 8 zero) x B bf16
+    assert M.lib.mhc_packed_weights_bytes(4, 5120) == (5120 // B) * 4 * 80 * B * 2
+    assert M.lib.mhc_packed_weights_bytes(4, B + 8) == 0
     assert M.lib.mhc_workspace_bytes(4, 5120) >= M.lib.mhc_packed_weights_bytes(4, 5120)
     assert M.lib.mhc_packed_weights_bytes(3, 5120) == 0
 
@@ -95,9 +99,11 @@ def test_fused_validation(M):
 
 
 def test_split_choices(M):
-    ok = {256: M.MHC_OK, 512: M.MHC_OK, 704: M.MHC_OK, 1024: M.MHC_OK, 2048: M.MHC_OK,
-          5120: M.MHC_OK, 5632: M.MHC_OK, 6144: M.MHC_ERR_SHAPE, 96: M.MHC_OK, 16: M.MHC_OK,
-          100: M.MHC_ERR_SHAPE, 7168: M.MHC_ERR_SHAPE}
+    B = M.lib.mhc_packed_block_columns()
+    ok = {4 * B: M.MHC_OK, 256: M.MHC_OK, 512: M.MHC_OK, 640: M.MHC_OK, 1024: M.MHC_OK,
+          2048: M.MHC_OK, 5120: M.MHC_OK, 704: M.MHC_ERR_SHAPE, 5632: M.MHC_ERR_SHAPE,
+          6144: M.MHC_ERR_SHAPE, 2 * B: M.MHC_ERR_SHAPE, 100: M.MHC_ERR_SHAPE,
+          7168: M.MHC_ERR_SHAPE}
     for d, want in ok.items():
         assert _fused(M, N=0, d=d, ws_bytes=1 << 40) == want, d
 
@@ -116,5 +122,6 @@ def test_other_calls_validation(M):
     assert lib.mhc_hc_post(*p[:5], 10, 2, 128, 0, None) == M.MHC_ERR_SHAPE
     assert lib.mhc_hc_pre(p[0], p[1], ctypes.c_void_p(p[0].value + 32), 10, 4, 128, None) == M.MHC_ERR_ALIAS
     assert lib.mhc_pack_weights(p[0], ctypes.c_void_p(p[0].value + 64), 4, 128, None) == M.MHC_ERR_ALIAS
+    assert lib.mhc_pack_weights(p[0], p[1], 4, 8, None) == M.MHC_ERR_SHAPE
     assert lib.mhc_mixes(*p[:8], 10, 4, 5120, 20, 1e-6, 1e-6, 0, None, 0, None) == M.MHC_ERR_WORKSPACE
     assert lib.mhc_mixes(*p[:8], 0, 4, 5120, 20, 1e-6, 1e-6, 0, p[7], 1 << 30, None) == M.MHC_OK

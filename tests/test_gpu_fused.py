@@ -42,7 +42,8 @@ CASES = [
     (300, 1024, 4),
     (260, 2048, 8),
     (300, 5120, 0),
-    (130, 5632, 8),          # widest slice that fits TMEM (704 columns)
+    (130, 640, 1),           # widest slice the TMEM stash ring holds (640 columns)
+    (260, 128, 1),           # narrowest slice (4 stages)
 ]
 
 

@@ -78,18 +78,30 @@ def test_hc_post_and_pre_bit_exact(M, synth, row_dest):
     assert_exact(to64(yh), O.hc_pre(ref, a["pre"]), "y_hat")
 
 
-def _planes(P):
-    """hi, mid, lo planes [24, K] from the packed layout (plane pl of row r at 36*(r//12)+12*pl+r%12)."""
-    rows = np.arange(24)
-    base = 36 * (rows // 12) + rows % 12
-    return P[base], P[base + 12], P[base + 24]
+def _planes(M, P, d):
+    """hi, mid, lo planes [24, 4d] decoded from the packed image documented at mhc_pack_weights:
+    d/B blocks of [4 streams][80 rows][B columns], plane pl of mix row r in row
+    36*(r//12)+12*pl+r%12, rows 72..79 zero, chunk c of row r stored at c ^ ((r*2B/128) % (B/8))."""
+    B = M.lib.mhc_packed_block_columns()
+    ch = B // 8
+    img = P.view(torch.bfloat16).float().cpu().numpy().reshape(d // B, 4, 80, ch, 8)
+    rows = np.arange(80)
+    phys = np.arange(ch)[None, :] ^ ((rows[:, None] * 2 * B // 128) % ch)    # [80, ch]
+    logical = np.take_along_axis(img, phys[None, None, :, :, None], axis=3)  # unswizzled
+    assert np.all(logical[:, :, 72:] == 0)
+    cols = logical.reshape(d // B, 4, 80, B).transpose(2, 1, 0, 3).reshape(80, 4 * d)
+    r = np.arange(24)
+    base = 36 * (r // 12) + r % 12
+    return cols[base], cols[base + 12], cols[base + 24]
 
 
 def test_pack_weights_reconstructs(M):
     g = torch.Generator(device=DEV).manual_seed(0)
     W = torch.randn(24, 4 * 512, generator=g, device=DEV) * 0.02
     W[0, :8] = torch.tensor([1e-30, -1e-30, 3.0e38, 0.0, -0.0, 1.0, 2.0 ** -126, 1e-40], device=DEV)
-    hi, mid, lo = _planes(M.pack_weights(W).double().cpu().numpy())
+    P = M.pack_weights(W)
+    assert P.numel() == M.packed_weights_bytes(512)
+    hi, mid, lo = _planes(M, P, 512)
     w = W.double().cpu().numpy()
     assert np.array_equal(hi, O.bf16_round(w))                # the hi plane is bf16(W)
     recon = (lo + mid) + hi
