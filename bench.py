@@ -249,6 +249,7 @@ def run_ours(args):
            "pre": torch.empty(N, 4, device=dev), "post": torch.empty(N, 4, device=dev),
            "comb": torch.empty(N, 4, 4, device=dev)}
     Wp = torch.empty(mhc.packed_weights_bytes(d), dtype=torch.uint8, device=dev)
+    scratch = torch.empty(mhc.step_scratch_bytes(d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev_a=None, ev_b=None):
@@ -256,8 +257,8 @@ def run_ours(args):
         if ev_a is not None:
             ev_a.record(stream)
         mhc.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None,
-                       inp["scale"], inp["base"], inp["gain"], W_packed=Wp, out=out,
-                       stream=stream)                                        # launch 2
+                       inp["scale"], inp["base"], inp["gain"], W_packed=Wp, scratch=scratch,
+                       out=out, stream=stream)                               # launch 2
         if ev_b is not None:
             ev_b.record(stream)
 
@@ -314,8 +315,8 @@ def run_ours(args):
                 dev_in[k].copy_(v, non_blocking=True)
             mhc.pack_weights(inp["W"], out=Wp, stream=stream)
             mhc.fused_step(dev_in["X"], dev_in["F"], dev_in["pre"], dev_in["post"], dev_in["comb"],
-                           None, inp["scale"], inp["base"], inp["gain"], W_packed=Wp, out=out,
-                           stream=stream)
+                           None, inp["scale"], inp["base"], inp["gain"], W_packed=Wp,
+                           scratch=scratch, out=out, stream=stream)
             for k, v in out.items():
                 host_out[k].copy_(v, non_blocking=True)
 

@@ -48,7 +48,7 @@ extern "C" {
  * the wait gives up, records MHC_ERR_TIMEOUT for mhc_get_status, and the call completes.      */
 #define MHC_DEBUG_NEVER_ARRIVE   0x2u
 /* Bits 8..11: number of CTAs (1, 2, 4 or 8) that split the width d of each token tile between
- * them (a thread-block cluster). 0 = automatic (the fewest that fit on chip).                  */
+ * them (a group of co-resident CTAs). 0 = automatic (the fewest that fit on chip).            */
 #define MHC_SPLIT_SHIFT          8
 #define MHC_SPLIT_MASK           (0xFu << MHC_SPLIT_SHIFT)
 
@@ -58,7 +58,12 @@ extern "C" {
 size_t mhc_packed_weights_bytes(int n, int d);
 /* Columns of d per block of the packed weights (B below).                                    */
 int mhc_packed_block_columns(void);
-/* Workspace of mhc_fused_step / mhc_mixes (the packed weights).                              */
+/* Scratch of the step kernel on the CURRENT device: the exchange area through which the CTAs
+ * that share a token tile sum their partial results (counters and partial sums; it grows with
+ * the device's SM count, about 4.4 MB on a 152-SM GB300). 0 if no device can be queried.     */
+size_t mhc_step_scratch_bytes(int n, int d);
+/* Workspace of mhc_fused_step / mhc_mixes on the current device: the packed weights (rounded
+ * up to 256 bytes) followed by the step scratch.                                             */
 size_t mhc_workspace_bytes(int n, int d);
 
 /* ---- the fused single-pass step ------------------------------------------------------------
@@ -88,7 +93,11 @@ size_t mhc_workspace_bytes(int n, int d);
  *   pre_out, post_out fp32 [N, n]; comb_out fp32 [N, n, n]; mixes_out fp32 [N, (2+n)n] or NULL
  *   d: for the chosen split, d/split must be a multiple of 2B (B = mhc_packed_block_columns())
  *      between 4B and 640 (d = 5120 uses split 8).
- *   workspace: >= mhc_workspace_bytes(n, d) device bytes; W_mix is packed into it each call.
+ *   workspace: >= mhc_workspace_bytes(n, d) device bytes; W_mix is packed into its start each
+ *      call and the rest is the step scratch. Calls that share a workspace or scratch buffer
+ *      must not overlap in time on the GPU (put them on one stream).
+ * The launch is cooperative (one CTA per SM, all resident); MHC_ERR_CUDA if the device cannot
+ * hold it (for example while other work occupies SMs of an MPS partition).
  * Returns MHC_OK or a negative code. N == 0 returns MHC_OK once the shape is valid, without
  * looking at the pointers (empty tensors may have none) and without launching.               */
 int mhc_fused_step(const void* X, const void* F, const float* pre_prev, const float* post_prev,
@@ -98,13 +107,15 @@ int mhc_fused_step(const void* X, const void* F, const float* pre_prev, const fl
                    int64_t N, int n, int d, int sinkhorn_iters, float hc_eps, float norm_eps,
                    unsigned flags, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Same step with W_mix already packed by mhc_pack_weights (no per-call packing).             */
+/* Same step with W_mix already packed by mhc_pack_weights (no per-call packing); `scratch` is
+ * >= mhc_step_scratch_bytes(n, d) device bytes.                                              */
 int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
                           const float* post_prev, const float* comb_prev, const void* W_packed,
                           const float* scale, const float* base, const float* gain, void* X_out,
                           void* y_out, float* pre_out, float* post_out, float* comb_out,
                           float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
-                          float hc_eps, float norm_eps, unsigned flags, void* stream);
+                          float hc_eps, float norm_eps, unsigned flags, void* scratch,
+                          size_t scratch_bytes, void* stream);
 
 /* ---- hc_mixes alone ------------------------------------------------------------------------
  * Stream weights for the feed-forward, Code: hc_mixes (+ the hc_split_sinkhorn kernel): from
@@ -156,9 +167,8 @@ int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* str
  * if the synchronisation itself failed.                                                       */
 int mhc_get_status(void* stream);
 /* Launch shape of the fused step on the current device: the width split it uses for (n, d,
- * flags) and how many such clusters the device can hold at once (cudaOccupancyMaxActiveClusters).
- * Diagnostic only; needs a GPU.                                                               */
-int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters);
+ * flags) and how many groups of `split` CTAs the device holds at once. Diagnostic; needs a GPU. */
+int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* groups);
 /* Phase tracing of the fused step (off by default). With a device buffer set, every later
  * launch whose grid fits records, per CTA, 8 uint64 values from the GPU's nanosecond timer:
  * the start time, then nanoseconds since the start at: loads issued, main loop done, partials

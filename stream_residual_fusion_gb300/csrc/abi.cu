@@ -82,12 +82,16 @@ int check_step_shape(int64_t N, int n, int d, int iters, unsigned flags, int* sp
   return *split == 0 ? MHC_ERR_SHAPE : MHC_OK;
 }
 
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// workspace = [packed weights | scratch]; W_mix given: pack into the workspace first.
 int fused_common(const void* X, const void* F, const float* pre_prev, const float* post_prev,
                  const float* comb_prev, const void* W_packed, const float* scale,
                  const float* base, const float* gain, void* X_out, void* y_out, float* pre_out,
                  float* post_out, float* comb_out, float* mixes_out, int64_t N, int n, int d,
                  int iters, float hc_eps, float norm_eps, unsigned flags, const void* workspace,
-                 uint64_t ws_bytes, const float* W_mix, void* stream) {
+                 uint64_t ws_bytes, void* scratch, uint64_t scratch_bytes, const float* W_mix,
+                 void* stream) {
   int split = 0;
   int rc = check_step_shape(N, n, d, iters, flags, &split);
   if (rc != MHC_OK) return rc;
@@ -95,8 +99,9 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
   if (!X || !F || !pre_prev || !post_prev || !comb_prev || !W_packed || !scale || !base || !gain ||
       !X_out || !y_out || !pre_out || !post_out || !comb_out)
     return MHC_ERR_NULL;
+  if (!scratch) return MHC_ERR_WORKSPACE;
   const void* ptrs[] = {X, F, pre_prev, post_prev, comb_prev, W_packed, scale, base, gain,
-                        X_out, y_out, pre_out, post_out, comb_out};
+                        X_out, y_out, pre_out, post_out, comb_out, scratch};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MHC_ERR_ALIGN;
   if (mixes_out && !aligned16(mixes_out)) return MHC_ERR_ALIGN;
@@ -110,12 +115,16 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
   const Span outs[] = {span(X_out, nt * K * 2), span(y_out, nt * d * 2), span(pre_out, nt * 16),
                        span(post_out, nt * 16), span(comb_out, nt * 64),
                        span(mixes_out, mixes_out ? nt * 96 : 0),
-                       span(workspace, workspace ? ws_bytes : 0)};
+                       span(workspace, workspace ? ws_bytes : 0),
+                       span(scratch, workspace ? 0 : scratch_bytes)};
   if (!aliasing_ok(outs, ins, 0, 0)) return MHC_ERR_ALIAS;
   if (!workspace) {  // pre-packed weights are an input too
     const Span packed_in[] = {span(W_packed, mhc_packed_weights_bytes(4, d))};
     if (!aliasing_ok(outs, packed_in)) return MHC_ERR_ALIAS;
   }
+  const size_t need = step_scratch_bytes();
+  if (need == 0) return MHC_ERR_CUDA;
+  if (scratch_bytes < need) return MHC_ERR_WORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (W_mix) {
@@ -138,6 +147,8 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
   a.post_out = post_out;
   a.comb_out = comb_out;
   a.mixes_out = mixes_out;
+  a.scratch = scratch;
+  a.scratch_bytes = scratch_bytes;
   a.N = N;
   a.d = d;
   a.split = split;
@@ -157,7 +168,16 @@ size_t mhc_packed_weights_bytes(int n, int d) {
   return static_cast<size_t>(d / STEP_DC) * STEP_WBLOCK_BYTES;
 }
 
-size_t mhc_workspace_bytes(int n, int d) { return mhc_packed_weights_bytes(n, d); }
+size_t mhc_step_scratch_bytes(int n, int d) {
+  if (mhc_packed_weights_bytes(n, d) == 0) return 0;
+  return step_scratch_bytes();
+}
+
+size_t mhc_workspace_bytes(int n, int d) {
+  const size_t packed = mhc_packed_weights_bytes(n, d);
+  if (packed == 0) return 0;
+  return align256(packed) + step_scratch_bytes();
+}
 
 int mhc_packed_block_columns(void) { return STEP_DC; }
 
@@ -181,10 +201,13 @@ int mhc_fused_step(const void* X, const void* F, const float* pre_prev, const fl
   if (rc != MHC_OK) return rc;
   if (N == 0) return MHC_OK;
   if (!W_mix) return MHC_ERR_NULL;
-  if (!workspace || workspace_bytes < mhc_workspace_bytes(n, d)) return MHC_ERR_WORKSPACE;
+  const size_t packed = align256(mhc_packed_weights_bytes(n, d));
+  if (!workspace || workspace_bytes < packed) return MHC_ERR_WORKSPACE;
   return fused_common(X, F, pre_prev, post_prev, comb_prev, workspace, scale, base, gain, X_out,
                       y_out, pre_out, post_out, comb_out, mixes_out, N, n, d, sinkhorn_iters,
-                      hc_eps, norm_eps, flags, workspace, workspace_bytes, W_mix, stream);
+                      hc_eps, norm_eps, flags, workspace, workspace_bytes,
+                      static_cast<uint8_t*>(workspace) + packed, workspace_bytes - packed, W_mix,
+                      stream);
 }
 
 int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
@@ -192,10 +215,12 @@ int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
                           const float* scale, const float* base, const float* gain, void* X_out,
                           void* y_out, float* pre_out, float* post_out, float* comb_out,
                           float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
-                          float hc_eps, float norm_eps, unsigned flags, void* stream) {
+                          float hc_eps, float norm_eps, unsigned flags, void* scratch,
+                          size_t scratch_bytes, void* stream) {
   return fused_common(X, F, pre_prev, post_prev, comb_prev, W_packed, scale, base, gain, X_out,
                       y_out, pre_out, post_out, comb_out, mixes_out, N, n, d, sinkhorn_iters,
-                      hc_eps, norm_eps, flags, nullptr, 0, nullptr, stream);
+                      hc_eps, norm_eps, flags, nullptr, 0, scratch, scratch_bytes, nullptr,
+                      stream);
 }
 
 int mhc_mixes(const void* X, const float* W_mix, const float* scale, const float* base,
@@ -208,7 +233,10 @@ int mhc_mixes(const void* X, const float* W_mix, const float* scale, const float
   if (N == 0) return MHC_OK;
   if (!X || !W_mix || !scale || !base || !pre_out || !post_out || !comb_out) return MHC_ERR_NULL;
   if (!workspace) return MHC_ERR_WORKSPACE;
-  if (workspace_bytes < mhc_workspace_bytes(n, d)) return MHC_ERR_WORKSPACE;
+  const size_t packed = align256(mhc_packed_weights_bytes(n, d));
+  const size_t need = step_scratch_bytes();
+  if (need == 0) return MHC_ERR_CUDA;
+  if (workspace_bytes < packed + need) return MHC_ERR_WORKSPACE;
   const void* ptrs[] = {X, W_mix, scale, base, pre_out, post_out, comb_out, workspace};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MHC_ERR_ALIGN;
@@ -230,6 +258,8 @@ int mhc_mixes(const void* X, const float* W_mix, const float* scale, const float
   a.post_out = post_out;
   a.comb_out = comb_out;
   a.mixes_out = mixes_out;
+  a.scratch = static_cast<uint8_t*>(workspace) + packed;
+  a.scratch_bytes = workspace_bytes - packed;
   a.N = N;
   a.d = d;
   a.split = split;

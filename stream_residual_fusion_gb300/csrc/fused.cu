@@ -5,10 +5,11 @@
 // from Stream weights for the feed-forward, Code; the single pass is the one that page's "Why"
 // section describes (one pass over the streams serves the read and the next weights).
 //
-// Work decomposition. A thread-block cluster of `split` CTAs owns a tile of 128 tokens at a time
-// and walks its tiles persistently (tile c, c + #clusters, ...):
+// Work decomposition. A group of `split` CTAs owns a tile of 128 tokens at a time and walks its
+// tiles persistently (tile c, c + #groups, ...). The launch is cooperative with one CTA per SM,
+// so every CTA of a group is resident and the groups use all SMs:
 //   * Each CTA owns d/split columns of every stream (d = 5120: 8 CTAs x 640 columns). The CTAs'
-//     columns interleave in steps of STEP_DC, so at every stage the cluster reads one contiguous
+//     columns interleave in steps of STEP_DC, so at every stage the group reads one contiguous
 //     run of STEP_DC*split columns of each token row.
 //   * Warp 0 drives a TMA ring: per stage [128 tokens x STEP_DC] tiles of X_0..X_3 and F (tensor
 //     copies) and the stage's block of packed projection weights (one contiguous bulk copy: the
@@ -22,9 +23,9 @@
 //     consumers fold each finished group into float32 running sums in shared memory.
 //   * Warp 10 stores X' and y with TMA straight from the stage's tiles and frees the stage as
 //     soon as the stores have read it.
-//   * After a tile's last stage the consumers post their slice's partial sums to the cluster
-//     (distributed shared memory, remote mbarrier arrivals); warp 11 finishes the tile's mix
-//     numbers (scale, split, Sinkhorn) while the consumers move on to the next tile.
+//   * After a tile's last stage the consumers post their slice's partial sums to the group
+//     through a scratch area in global memory (L2) and release-ordered counters; warp 11
+//     finishes the tile's mix numbers (scale, split, Sinkhorn) while the consumers move on.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -70,7 +71,7 @@ constexpr int PART_BYTES = TT * PART_STRIDE * 4;   // one tile's running sums; t
 constexpr int OFF_PART = NSTAGE * STAGE_BYTES;
 constexpr int OFF_RY = OFF_PART + 2 * PART_BYTES;
 constexpr int OFF_BARS = OFF_RY + TT * 4;
-constexpr int NBARS = 3 * NSTAGE + 10;  // full/empty/xready per stage; accready, pready, pfree, syready [2]; drained; never
+constexpr int NBARS = 3 * NSTAGE + 4;   // full/empty/xready per stage; accready[2]; drained; never
 constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;   // + slack for 1 KB alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -101,6 +102,8 @@ struct StepParams {
   float* mixes_out;
   unsigned* status;
   unsigned long long* trace;   // optional: 8 phase timestamps per (tile, CTA) (mhc_set_trace)
+  unsigned* counters;          // per group: syready[2], pready[2], pfree[2] (zeroed per launch)
+  float* gpart;                // per group: [2 buffers][split ranks][TT tokens][PART_STRIDE]
   int N;
   int d;
   int split;
@@ -175,7 +178,7 @@ __device__ __forceinline__ void stash_store(uint32_t taddr, const uint32_t (&w)[
   }
 }
 
-// Persistent: cluster c of `gridDim.y` clusters handles tiles c, c + gridDim.y, ... The TMA ring,
+// Persistent: group c of gridDim.x / split groups handles tiles c, c + #groups, ... The TMA ring,
 // the accumulation groups and the barrier phases run on across tiles.
 template <bool FUSED>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -189,21 +192,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* empty = full + NSTAGE;
   uint64_t* xready = empty + NSTAGE;
   uint64_t* accready = xready + NSTAGE;     // [2]: an accumulation group finished in buffer i
-  uint64_t* pready = accready + 2;          // [2]: every CTA of the cluster posted partials[i]
-  uint64_t* pfree = pready + 2;             // [2]: every CTA's finisher has read partials[i]
-  uint64_t* syready = pfree + 2;            // [2]: every CTA posted the y_hat sums of squares[i]
-  uint64_t* drained = syready + 2;          // the last X'/y stores have left the ring
+  uint64_t* drained = accready + 2;         // the last X'/y stores have left the ring
   uint64_t* never = drained + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
   float* ry = reinterpret_cast<float*>(sm + OFF_RY);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t g = cluster_ctarank();
   const int split = P.split;
+  const uint32_t g = blockIdx.x % split;              // rank within the group
   const int ntiles = (P.N + TT - 1) / TT;
-  const int nclust = gridDim.y;
-  const int c0 = blockIdx.y;
+  const int nclust = gridDim.x / split;               // groups
+  const int c0 = blockIdx.x / split;                  // this CTA's group = its first tile
+  // group exchange (global memory): counters and the partial sums of every rank
+  unsigned* const syready = P.counters + 8 * c0;      // [2]: consumer warps that posted S_x, S_y
+  unsigned* const pready = syready + 2;               // [2]: consumer warps that posted mix sums
+  unsigned* const pfree = syready + 4;                // [2]: finishers done reading a buffer
+  auto gpart = [&](int pb, int rank) {
+    return P.gpart + ((static_cast<size_t>(c0) * 2 + pb) * split + rank) * (TT * PART_STRIDE);
+  };
   const int col0 = static_cast<int>(g) * DC;          // first column of this CTA's slice
   const int cstride = DC * split;                     // stride between its stages' columns
   const int S = P.nsteps;
@@ -214,7 +221,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto limit = [&]() { return timed_out ? 0ull : WAIT_LIMIT_NS; };
 
   // optional phase trace, one record per (tile, rank): slot 0 absolute tile start; slots 1..6
-  // ns since then: producer done, loop done, partials posted, cluster partials ready, finisher
+  // ns since then: producer done, loop done, partials posted, (unused), finisher
   // done, consumers' tile end; slot 7 = SM id << 40 | ns to the kernel end.
   auto trace_rec = [&](int tile) -> unsigned long long* {
     return P.trace == nullptr ? nullptr : P.trace + 8ull * (static_cast<unsigned long long>(tile) * split + g);
@@ -228,12 +235,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     mbar_init(&accready[0], 1);
     mbar_init(&accready[1], 1);
-    mbar_init(&pready[0], split * NCONS);
-    mbar_init(&pready[1], split * NCONS);
-    mbar_init(&pfree[0], split);
-    mbar_init(&pfree[1], split);
-    mbar_init(&syready[0], split * NCONS);
-    mbar_init(&syready[1], split * NCONS);
     mbar_init(drained, 1);
     mbar_init(never, 1);
     fence_mbar_init();
@@ -244,7 +245,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();               // peers' barriers are initialised before anyone arrives on them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -373,13 +373,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // RMS factor of tile iteration it_ for this token: y_hat sums of squares of every slice
     auto rms_factor = [&](int it_) {
-      if (!mbar_wait_cluster(&syready[it_ & 1], (it_ >> 1) & 1, limit())) timed_out = true;
+      const unsigned target = static_cast<unsigned>(((it_ >> 1) + 1) * split * NCONS);
+      if (!gwait(&syready[it_ & 1], target, limit())) timed_out = true;
       float v[8];
-      const uint32_t local = smem_u32(part_of(it_) + 24);   // (S_x h0, S_x h1, S_y h0, S_y h1)
 #pragma unroll
-      for (int rk = 0; rk < 8; ++rk) {
+      for (int rk = 0; rk < 8; ++rk) {   // row tail (S_x h0, S_x h1, S_y h0, S_y h1) of every rank
         if (rk < split) {
-          const float4 q4 = ld_cluster_f32x4(map_cluster(local, rk));
+          const float4 q4 = __ldcg(reinterpret_cast<const float4*>(gpart(it_ & 1, rk) + tl * PART_STRIDE + 24));
           v[rk] = q4.z + q4.w;
         } else {
           v[rk] = 0.f;
@@ -390,17 +390,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return f2{r, r};
     };
     // fold accumulation group gg into its tile's running sums; after a tile's last group, post
-    // the tile's partials to every CTA of the cluster
+    // the tile's partials to the group
     auto fold = [&](int gg) {
       if (!mbar_wait(&accready[gg & 1], (gg >> 1) & 1, limit())) timed_out = true;
       tc_fence_after();
       const int it_ = gg / G;
-      fold_group(lane_base, gg, h, part_of(it_) + 12 * h);
+      float* run = part_of(it_) + 12 * h;
+      fold_group(lane_base, gg, h, run);
       if (gg % G == G - 1) {
-        // this warp's share of the tile's partial sums is final: tell every CTA of the cluster
-        // (the remote arrive releases at cluster scope what the warp wrote before __syncwarp)
+        // this thread's 12 mix sums of the tile are final: publish them to the group (the
+        // counter's release orders what the warp wrote before __syncwarp)
+        float4* dst = reinterpret_cast<float4*>(gpart(it_ & 1, g) + tl * PART_STRIDE + 12 * h);
+        const float4* src = reinterpret_cast<const float4*>(run);
+        dst[0] = src[0];
+        dst[1] = src[1];
+        dst[2] = src[2];
         __syncwarp();
-        if (lane < split) mbar_arrive_remote(&pready[it_ & 1], lane);
+        if (lane == 0) gcount_release(&pready[it_ & 1]);
         if (warp == NROLE && lane == 0) {
           if (auto tr = trace_rec(c0 + it_ * nclust)) tr[3] = global_timer_ns() - tr[0];
         }
@@ -409,7 +415,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     load_coeffs(c0);
 
     // RMS factors: r_old for tile it-2 (consumed in stages 0, 1), r_new for tile it-1 (from
-    // stage 2 on; computed there, two stages after the cluster posted it)
+    // stage 2 on; computed there, two stages after the group posted it)
     f2 r_old{0.f, 0.f}, r_new{0.f, 0.f};
     int gs = 0, it = 0, folded = 0;
     int slot = 0;                        // gs % R, kept incrementally
@@ -417,8 +423,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float* run = part_of(it) + 12 * h;
       unsigned long long* tr = trace_rec(tile);
       if (warp == NROLE && lane == 0 && tr) tr[0] = global_timer_ns();
-      // partials[it & 1] was last used two tiles ago: wait until every finisher has read it
-      if (it >= 2 && !mbar_wait_cluster(&pfree[it & 1], ((it >> 1) - 1) & 1, limit())) timed_out = true;
       reinterpret_cast<float4*>(run)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       reinterpret_cast<float4*>(run)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       reinterpret_cast<float4*>(run)[2] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -530,16 +534,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (tr && warp == NROLE && lane == 0) tr[2] = global_timer_ns() - tr[0];
 
       // ------------------------------------------------------------ post this slice's sums
-      // row layout: [0..23] mix sums (half h owns 12h..12h+11), [24 + h] S_x, [26 + h] S_y
+      // row layout: [0..23] mix sums (half h owns 12h..12h+11), [24 + h] S_x, [26 + h] S_y.
+      // The group buffer it & 1 was last read (by every finisher) two tiles ago.
+      if (it >= 2 && !gwait(&pfree[it & 1], static_cast<unsigned>((it >> 1) * split), limit()))
+        timed_out = true;
       {
-        float* pt = part_of(it);
+        float* pt = gpart(it & 1, g) + tl * PART_STRIDE;
         pt[24 + h] = sx2.x + sx2.y;
         pt[26 + h] = sy2.x + sy2.y;
       }
-      if (FUSED) {
-        __syncwarp();
-        if (lane < split) mbar_arrive_remote(&syready[it & 1], lane);
-      }
+      __syncwarp();
+      if (FUSED && lane == 0) gcount_release(&syready[it & 1]);
       load_coeffs(tile + nclust);
       if (tr && warp == NROLE && lane == 0) tr[6] = global_timer_ns() - tr[0];
     }
@@ -589,8 +594,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int it = 0;
     for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
       const int pb = it & 1;
-      const float* part = reinterpret_cast<const float*>(sm + OFF_PART + pb * PART_BYTES);
-      if (!mbar_wait_cluster(&pready[pb], (it >> 1) & 1, limit())) timed_out = true;
+      if (!gwait(&pready[pb], static_cast<unsigned>(((it >> 1) + 1) * split * NCONS), limit()))
+        timed_out = true;
       const int t0 = tile * TT;
       // 16 tokens per pass (two per lane group); after the last pass's reads the peers may
       // reuse their partials buffers
@@ -600,13 +605,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int u = 0; u < 2; ++u) {
           s0[u] = s1[u] = s2[u] = s6[u] = make_float4(0.f, 0.f, 0.f, 0.f);
           const int tl2 = static_cast<int>(g) * per + min(base_t + 8 * u + q, per - 1);
-          const uint32_t local = smem_u32(part + tl2 * PART_STRIDE);
           for (int rk = 0; rk < split; ++rk) {
-            const uint32_t ra = map_cluster(local, rk);
-            const float4 v0 = ld_cluster_f32x4(ra);
-            const float4 v1 = ld_cluster_f32x4(ra + 16);
-            const float4 v2 = ld_cluster_f32x4(ra + 16 * (2 + j));
-            const float4 v6 = ld_cluster_f32x4(ra + 16 * 6);
+            const float4* row = reinterpret_cast<const float4*>(gpart(pb, rk) + tl2 * PART_STRIDE);
+            const float4 v0 = __ldcg(row);
+            const float4 v1 = __ldcg(row + 1);
+            const float4 v2 = __ldcg(row + 2 + j);
+            const float4 v6 = __ldcg(row + 6);
             s0[u].x += v0.x; s0[u].y += v0.y; s0[u].z += v0.z; s0[u].w += v0.w;
             s1[u].x += v1.x; s1[u].y += v1.y; s1[u].z += v1.z; s1[u].w += v1.w;
             s2[u].x += v2.x; s2[u].y += v2.y; s2[u].z += v2.z; s2[u].w += v2.w;
@@ -614,9 +618,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         if (base_t + 16 >= per) {
-          // every read of partials[pb] is done: tell every CTA of the cluster it may reuse it
+          // every read of buffer pb is done: the group may reuse it
           __syncwarp();
-          if (lane < split) mbar_arrive_remote(&pfree[pb], lane);
+          if (lane == 0) gcount_release(&pfree[pb]);
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -658,7 +662,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // ------------------------------------------------------------------ leave together
   tc_fence_before();
   __syncthreads();
-  cluster_sync();               // no CTA leaves while a peer may still read its partials
   if (threadIdx.x == 0 && P.trace != nullptr) {
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -718,29 +721,23 @@ bool map_rows(CUtensorMap* m, const void* p, int64_t rows, int64_t cols, uint32_
 }
 
 
+// CTAs of the step kernel the current device holds at once (one per SM).
 template <typename Kern>
-cudaError_t step_occupancy_of(Kern kern, int split, int* clusters) {
-  // cached per (kernel, split): the query costs a few microseconds
-  static int cache[2][9] = {};
+cudaError_t resident_ctas(Kern kern, int* ctas) {
+  static int cache[2] = {0, 0};
   const int which = (kern == step_kernel<true>) ? 1 : 0;
-  if (split >= 1 && split <= 8 && cache[which][split] > 0) {
-    *clusters = cache[which][split];
+  if (cache[which] > 0) {
+    *ctas = cache[which];
     return cudaSuccess;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(split, 1024, 1);
-  cfg.blockDim = dim3(NTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaOccupancyMaxActiveClusters(clusters, kern, &cfg);
-  if (e == cudaSuccess && split >= 1 && split <= 8) cache[which][split] = *clusters;
-  return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NTHREADS, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cache[which] = sms * per_sm;
+  *ctas = cache[which];
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -757,6 +754,16 @@ int choose_split(int d, int forced) {
   return 0;
 }
 
+size_t step_scratch_bytes() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  // per CTA (at most one per SM): its group's counters (32 bytes, shared by the group) and two
+  // buffers of its partial sums
+  return 256 + static_cast<size_t>(sms) * (32 + 2 * PART_BYTES);
+}
+
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   CUtensorMap tx, tf, txo, ty;
   if (!map_streams(&tx, a.X, a.N, a.d)) return cudaErrorInvalidValue;
@@ -769,6 +776,16 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
     txo = tx;
     ty = tx;
   }
+  auto kern = fused ? step_kernel<true> : step_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int ctas = 0;
+  e = resident_ctas(kern, &ctas);
+  if (e != cudaSuccess) return e;
+  const int tiles = static_cast<int>((a.N + TT - 1) / TT);
+  const int ngroups = std::max(1, std::min(tiles, ctas / a.split));
+  if (ctas < a.split) return cudaErrorInvalidConfiguration;
+
   StepParams P{};
   P.pre_prev = a.pre_prev;
   P.post_prev = a.post_prev;
@@ -783,7 +800,14 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   P.mixes_out = a.mixes_out;
   P.status = status_word();
   if (P.status == nullptr) return cudaErrorInvalidDevice;
-  P.trace = trace_buffer(static_cast<int64_t>(a.split) * ((a.N + TT - 1) / TT));
+  P.trace = trace_buffer(static_cast<int64_t>(a.split) * tiles);
+  // scratch: [256 B of group counters per 8 groups ... ] then the partial sums
+  uint8_t* scratch = static_cast<uint8_t*>(a.scratch);
+  const size_t counter_bytes = (static_cast<size_t>(ngroups) * 32 + 255) / 256 * 256;
+  P.counters = reinterpret_cast<unsigned*>(scratch);
+  P.gpart = reinterpret_cast<float*>(scratch + counter_bytes);
+  if (counter_bytes + static_cast<size_t>(ngroups) * a.split * 2 * PART_BYTES > a.scratch_bytes)
+    return cudaErrorInvalidValue;
   P.N = static_cast<int>(a.N);
   P.d = a.d;
   P.split = a.split;
@@ -794,34 +818,29 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   P.norm_eps = a.norm_eps;
   P.flags = a.flags;
 
-  auto kern = fused ? step_kernel<true> : step_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  e = cudaMemsetAsync(P.counters, 0, static_cast<size_t>(ngroups) * 32, stream);
   if (e != cudaSuccess) return e;
-  const int tiles = static_cast<int>((a.N + TT - 1) / TT);
-  int resident = 0;
-  e = step_occupancy_of(kern, a.split, &resident);
-  if (e != cudaSuccess) return e;
-  const int nclust = std::max(1, std::min(tiles, resident));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.split, nclust, 1);
+  cfg.gridDim = dim3(ngroups * a.split, 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: groups wait on each other
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tx, tf, txo, ty, P);
 }
 
-cudaError_t step_occupancy(int split, int* clusters) {
+cudaError_t step_occupancy(int split, int* groups) {
   auto kern = step_kernel<true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return step_occupancy_of(kern, split, clusters);
+  int ctas = 0;
+  e = resident_ctas(kern, &ctas);
+  if (e == cudaSuccess) *groups = ctas / split;
+  return e;
 }
 
 }  // namespace mhc

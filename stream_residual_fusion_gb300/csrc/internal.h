@@ -28,6 +28,8 @@ struct StepArgs {
   float* post_out;
   float* comb_out;
   float* mixes_out;         // nullable
+  void* scratch;            // group exchange area, >= step_scratch_bytes()
+  size_t scratch_bytes;
   int64_t N;
   int d;
   int split;                // CTAs per token tile (cluster size)
@@ -43,7 +45,9 @@ int choose_split(int d, int forced);
 constexpr int kMaxTokens = 65535 * 128;
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream);
-cudaError_t step_occupancy(int split, int* clusters);
+cudaError_t step_occupancy(int split, int* groups);
+// Scratch the step kernel needs on the current device (0 if the device cannot be queried).
+size_t step_scratch_bytes();
 cudaError_t launch_pack(const float* W, void* packed, int d, cudaStream_t stream);
 cudaError_t launch_sinkhorn(const float* mixes, const float* scale, const float* base, float* pre,
                             float* post, float* comb, int64_t N, int iters, float eps,

@@ -375,6 +375,30 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// global-memory counters between co-resident CTAs (cooperative launch)
+
+// counter += 1 with release semantics at GPU scope: writes this thread made, and those it has
+// synchronised with, are visible to a thread that observes the new count with acquire.
+__device__ __forceinline__ void gcount_release(unsigned* ctr) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+}
+__device__ __forceinline__ unsigned gload_acquire(const unsigned* ctr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  return v;
+}
+// Waits until *ctr >= target, polling every ~128 ns, giving up after limit_ns.
+__device__ __forceinline__ bool gwait(const unsigned* ctr, unsigned target, uint64_t limit_ns) {
+  if (static_cast<int>(gload_acquire(ctr) - target) >= 0) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(128);
+    if (static_cast<int>(gload_acquire(ctr) - target) >= 0) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
 // named barriers (a subset of the block's warps)
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

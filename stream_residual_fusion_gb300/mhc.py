@@ -54,7 +54,8 @@ SIGNATURES = {
     "mhc_workspace_bytes": (_SZ, [_I, _I]),
     "mhc_packed_block_columns": (_I, []),
     "mhc_fused_step": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
-    "mhc_fused_step_packed": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P]),
+    "mhc_fused_step_packed": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
+    "mhc_step_scratch_bytes": (_SZ, [_I, _I]),
     "mhc_mixes": (_I, [_P] * 8 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_sinkhorn": (_I, [_P] * 6 + [_I64, _I, _I, _F, _P]),
     "mhc_rmsnorm": (_I, [_P] * 3 + [_I64, _I, _F, _P]),
@@ -122,6 +123,10 @@ def packed_weights_bytes(d: int, n: int = N_STREAMS) -> int:
     return int(lib.mhc_packed_weights_bytes(n, d))
 
 
+def step_scratch_bytes(d: int, n: int = N_STREAMS) -> int:
+    return int(lib.mhc_step_scratch_bytes(n, d))
+
+
 # ---------------------------------------------------------------------------------------------
 # the calls
 
@@ -151,9 +156,10 @@ def _step_outputs(X, out, with_mixes):
 
 def fused_step(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, iters=20,
                hc_eps=1e-6, norm_eps=1e-6, flags=0, with_mixes=False, out=None, workspace=None,
-               W_packed=None, stream=None):
+               W_packed=None, scratch=None, stream=None):
     """One fused single-pass mHC step (mhc_fused_step, or mhc_fused_step_packed when
-    `W_packed` is given). Returns dict with Xp, y, pre, post, comb (and mixes)."""
+    `W_packed` is given; then `scratch` is its step scratch). Returns dict with Xp, y, pre,
+    post, comb (and mixes)."""
     _need(X, torch.bfloat16, "X")
     _need(F, torch.bfloat16, "F")
     for t, nm in ((pre_prev, "pre_prev"), (post_prev, "post_prev"), (comb_prev, "comb_prev"),
@@ -165,10 +171,12 @@ def fused_step(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, it
                   _ptr(o.get("mixes"))]
     if W_packed is not None:
         _need(W_packed, torch.uint8, "W_packed")
+        if scratch is None:
+            scratch = torch.empty(step_scratch_bytes(d, n), dtype=torch.uint8, device=X.device)
         rc = lib.mhc_fused_step_packed(
             _ptr(X), _ptr(F), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev), _ptr(W_packed),
             _ptr(scale), _ptr(base), _ptr(gain), *common_out, N, n, d, iters, hc_eps, norm_eps,
-            flags, _stream(stream))
+            flags, _ptr(scratch), scratch.numel(), _stream(stream))
         _check(rc, "mhc_fused_step_packed")
     else:
         _need(W, torch.float32, "W")
