@@ -117,6 +117,29 @@ int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
                           float hc_eps, float norm_eps, unsigned flags, void* scratch,
                           size_t scratch_bytes, void* stream);
 
+/* ---- the fused step without any allocation --------------------------------------------------
+ * No counterpart in the paper: an addition for callers that cannot allocate device memory when
+ * they run the step (code being captured into a CUDA graph or stream that must not allocate, a
+ * serving loop with a fixed memory budget or an allocator it cannot call, a plain C host with no
+ * allocator of its own). Same arguments and results as mhc_fused_step, without the workspace:
+ * the packed weights and the step scratch live in one fixed array of
+ * mhc_noalloc_scratch_bytes() (8 MiB) that the library keeps on every GPU that loads it until
+ * the process exits. No device memory is allocated or freed, by this call or by anything it
+ * calls. Returns MHC_ERR_WORKSPACE when the packed weights for d plus the step scratch for the
+ * current device do not fit that array (n = 4: d <= 5120 fits on devices of up to 178 SMs).
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture. All calls on a device share the array and leave
+ * the last call's contents in it (the step clears what it needs zeroed), so calls that overlap
+ * on the GPU -- on different streams, or from different threads -- race: serialise them.   */
+int mhc_fused_step_noalloc(const void* X, const void* F, const float* pre_prev,
+                           const float* post_prev, const float* comb_prev, const float* W_mix,
+                           const float* scale, const float* base, const float* gain, void* X_out,
+                           void* y_out, float* pre_out, float* post_out, float* comb_out,
+                           float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
+                           float hc_eps, float norm_eps, unsigned flags, void* stream);
+/* Bytes of the fixed per-device array mhc_fused_step_noalloc uses.                          */
+size_t mhc_noalloc_scratch_bytes(void);
+
 /* ---- hc_mixes alone ------------------------------------------------------------------------
  * Stream weights for the feed-forward, Code: hc_mixes (+ the hc_split_sinkhorn kernel): from
  * bf16 streams X [N,n,d], the 24 mix numbers m (optional output) and pre/post/comb as above.

@@ -365,6 +365,72 @@ int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters) 
   return cuda_code(step_occupancy(sp, clusters));
 }
 
+// ---------------------------------------------------------------------------------------------
+// Allocation-free fused step.
+//
+// Some callers cannot allocate device memory at the point they run the step: code inside a
+// CUDA-graph or stream capture that must not allocate, a serving loop running under a fixed
+// memory budget or a caching allocator it cannot enter, or a plain C host that links this
+// library and has no allocator of its own. This entry point runs the same fused step with its
+// scratch (the packed weights and the step's exchange area) in one fixed array that the
+// library holds on every GPU that loads it, until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the fixed scratch on the current device (set up once per device).
+void* noalloc_scratch(int* rc) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *rc = MHC_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      *rc = MHC_ERR_CUDA;
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *rc = MHC_OK;
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+size_t mhc_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+int mhc_fused_step_noalloc(const void* X, const void* F, const float* pre_prev,
+                           const float* post_prev, const float* comb_prev, const float* W_mix,
+                           const float* scale, const float* base, const float* gain, void* X_out,
+                           void* y_out, float* pre_out, float* post_out, float* comb_out,
+                           float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
+                           float hc_eps, float norm_eps, unsigned flags, void* stream) {
+  int split = 0;
+  int rc = check_step_shape(N, n, d, sinkhorn_iters, flags, &split);
+  if (rc != MHC_OK) return rc;
+  if (N == 0) return MHC_OK;
+  if (!W_mix) return MHC_ERR_NULL;
+  const size_t need = mhc_workspace_bytes(n, d);
+  if (need == 0) return MHC_ERR_CUDA;
+  if (need > kNoAllocScratchBytes) return MHC_ERR_WORKSPACE;   // beyond the fixed scratch
+  void* ws = noalloc_scratch(&rc);
+  if (ws == nullptr) return rc;
+  const size_t packed = align256(mhc_packed_weights_bytes(n, d));
+  return fused_common(X, F, pre_prev, post_prev, comb_prev, ws, scale, base, gain, X_out, y_out,
+                      pre_out, post_out, comb_out, mixes_out, N, n, d, sinkhorn_iters, hc_eps,
+                      norm_eps, flags, ws, kNoAllocScratchBytes,
+                      static_cast<uint8_t*>(ws) + packed, kNoAllocScratchBytes - packed, W_mix,
+                      stream);
+}
+
 int mhc_set_trace(void* buffer, int64_t bytes) {
   if (buffer != nullptr && (!aligned16(buffer) || bytes < 64)) return MHC_ERR_ALIGN;
   g_trace = static_cast<unsigned long long*>(buffer);

@@ -56,6 +56,8 @@ SIGNATURES = {
     "mhc_fused_step": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_fused_step_packed": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_step_scratch_bytes": (_SZ, [_I, _I]),
+    "mhc_fused_step_noalloc": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P]),
+    "mhc_noalloc_scratch_bytes": (_SZ, []),
     "mhc_mixes": (_I, [_P] * 8 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_sinkhorn": (_I, [_P] * 6 + [_I64, _I, _I, _F, _P]),
     "mhc_rmsnorm": (_I, [_P] * 3 + [_I64, _I, _F, _P]),
@@ -187,6 +189,28 @@ def fused_step(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, it
             _ptr(scale), _ptr(base), _ptr(gain), *common_out, N, n, d, iters, hc_eps, norm_eps,
             flags, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
         _check(rc, "mhc_fused_step")
+    return o
+
+
+def fused_step_noalloc(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, iters=20,
+                       hc_eps=1e-6, norm_eps=1e-6, flags=0, with_mixes=False, out=None,
+                       stream=None):
+    """mhc_fused_step_noalloc: the fused step with the library's fixed per-device scratch, for
+    callers that cannot allocate device memory when the step runs. Only the outputs are
+    allocated here (pass `out` to allocate nothing)."""
+    _need(X, torch.bfloat16, "X")
+    _need(F, torch.bfloat16, "F")
+    for t, nm in ((pre_prev, "pre_prev"), (post_prev, "post_prev"), (comb_prev, "comb_prev"),
+                  (W, "W"), (scale, "scale"), (base, "base"), (gain, "gain")):
+        _need(t, torch.float32, nm)
+    N, n, d = X.shape
+    o = _step_outputs(X, out, with_mixes)
+    rc = lib.mhc_fused_step_noalloc(
+        _ptr(X), _ptr(F), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev), _ptr(W), _ptr(scale),
+        _ptr(base), _ptr(gain), _ptr(o["Xp"]), _ptr(o["y"]), _ptr(o["pre"]), _ptr(o["post"]),
+        _ptr(o["comb"]), _ptr(o.get("mixes")), N, n, d, iters, hc_eps, norm_eps, flags,
+        _stream(stream))
+    _check(rc, "mhc_fused_step_noalloc")
     return o
 
 
