@@ -238,6 +238,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     from stream_residual_fusion_gb300 import mhc, synth
+    from stream_residual_fusion_gb300.dist import max_over_ranks, weak_scaling_throughput
     w = synth.WORKLOADS[WORKLOAD]
     N, d = w.N, w.d
     inp = synth.make_workload(w, seed=3000 + rank, device=dev)
@@ -293,12 +294,9 @@ def run_ours(args):
     total_ms = t_start.elapsed_time(t_end)
     fused_ms = [a.elapsed_time(b) for a, b in ev]
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device=dev)          # the slowest rank's time
     ms_per_step = total_ms / K
-    value = world * N / (ms_per_step / 1e3)
+    value = weak_scaling_throughput(N, world, ms_per_step / 1e3)
 
     # ------------------------------------------------------------------ end to end, host buffers
     e2e = None
@@ -330,12 +328,10 @@ def run_ours(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        te = torch.tensor([a.elapsed_time(b) / e2e_steps], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * N / (float(te.item()) / 1e3), "unit": "tokens/s",
+        te = max_over_ranks(a.elapsed_time(b) / e2e_steps, device=dev)
+        e2e = {"value": weak_scaling_throughput(N, world, te / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": float(te.item()), "steps": e2e_steps}
+               "ms_per_step": te, "steps": e2e_steps}
         del host, host_out, dev_in
 
     if rank != 0:
