@@ -156,7 +156,7 @@ def _oracle_chunk(args):
     return hi - lo, time.perf_counter() - t0
 
 
-def oracle_throughput(tokens_per_worker: int = 96):
+def oracle_throughput(tokens_per_worker: int = 256):
     """The oracle, as it stands, on a bounded sample of the workload: one spawned single-threaded
     process per host core, each on its own slice of tokens. Returns (tokens/s, cores, sample)."""
     import multiprocessing as mp
