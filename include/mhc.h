@@ -140,6 +140,38 @@ int mhc_fused_step_noalloc(const void* X, const void* F, const float* pre_prev,
 /* Bytes of the fixed per-device array mhc_fused_step_noalloc uses.                          */
 size_t mhc_noalloc_scratch_bytes(void);
 
+/* ---- the fused step on host-resident streams -------------------------------------------------
+ * No counterpart in the paper (its step runs on device tensors): the same step as
+ * mhc_fused_step for a caller whose per-token tensors are in HOST memory. The tokens are cut
+ * into chunks of chunk_tokens; chunk i is copied into device staging slot i%2, stepped, and
+ * copied back, on three internal streams of the current device, so that the host->device copy
+ * of chunk i+1, the step on chunk i and the device->host copy of chunk i-1 overlap. The
+ * internal streams start after the work already queued on `stream`, and `stream` continues only
+ * after the last output has reached the host: synchronise `stream` before reading the outputs
+ * or reusing the inputs.
+ *   X, F, pre_prev, post_prev, comb_prev   HOST pointers, layouts as for mhc_fused_step
+ *   X_out, y_out, pre_out, post_out, comb_out, mixes_out (or NULL)   HOST pointers, same layouts;
+ *        X_out may equal X (chunk i's inputs are read before its outputs are written), no other
+ *        overlap (not checked on the host side). Page-locked (pinned) host memory is needed for
+ *        the copies to overlap; pageable memory gives the same results, serialised.
+ *   W_mix, scale, base, gain   DEVICE pointers (parameters stay resident on the GPU).
+ *   staging: >= mhc_host_staging_bytes(n, d, chunk_tokens, mixes_out != NULL) device bytes,
+ *        256-byte aligned (MHC_ERR_ALIGN otherwise): the workspace of mhc_fused_step followed by
+ *        two slots of chunk_tokens tokens' inputs and outputs.
+ * The internal streams and events are shared by all calls on a device: calls that overlap in
+ * time -- from different threads, or on different caller streams -- must be serialised.
+ * Returns MHC_OK or a negative code (as mhc_fused_step; MHC_ERR_SHAPE also for chunk_tokens
+ * < 1). An error returned part way leaves the chunks already queued to complete.          */
+int mhc_fused_step_host(const void* X, const void* F, const float* pre_prev,
+                        const float* post_prev, const float* comb_prev, const float* W_mix,
+                        const float* scale, const float* base, const float* gain, void* X_out,
+                        void* y_out, float* pre_out, float* post_out, float* comb_out,
+                        float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
+                        float hc_eps, float norm_eps, unsigned flags, void* staging,
+                        size_t staging_bytes, int64_t chunk_tokens, void* stream);
+/* Device bytes of the staging buffer of mhc_fused_step_host; 0 for an invalid shape or chunk. */
+size_t mhc_host_staging_bytes(int n, int d, int64_t chunk_tokens, int with_mixes);
+
 /* ---- hc_mixes alone ------------------------------------------------------------------------
  * Stream weights for the feed-forward, Code: hc_mixes (+ the hc_split_sinkhorn kernel): from
  * bf16 streams X [N,n,d], the 24 mix numbers m (optional output) and pre/post/comb as above.

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmhc.so")
-SOURCES = ["fused.cu", "small.cu", "abi.cu"]
+SOURCES = ["fused.cu", "small.cu", "abi.cu", "host_pipeline.cu"]
 HEADERS = ["ptx.cuh", "mix_math.cuh", "internal.h", "layout.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -23,31 +23,6 @@ int64_t g_trace_ctas = 0;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-struct Span {
-  uintptr_t lo, hi;
-  bool empty() const { return hi <= lo; }
-};
-Span span(const void* p, uint64_t bytes) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  return Span{a, a + static_cast<uintptr_t>(bytes)};
-}
-bool overlap(Span a, Span b) { return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi; }
-
-// Outputs must not overlap inputs or each other; (out i, in j) pairs listed in `same_ok` may be
-// exactly equal (same start and size).
-template <int NO, int NI>
-bool aliasing_ok(const Span (&outs)[NO], const Span (&ins)[NI], int same_out = -1, int same_in = -1) {
-  for (int i = 0; i < NO; ++i) {
-    for (int j = 0; j < NI; ++j) {
-      if (i == same_out && j == same_in && outs[i].lo == ins[j].lo && outs[i].hi == ins[j].hi) continue;
-      if (overlap(outs[i], ins[j])) return false;
-    }
-    for (int j = i + 1; j < NO; ++j)
-      if (overlap(outs[i], outs[j])) return false;
-  }
-  return true;
-}
-
 int cuda_code(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
 
 }  // namespace

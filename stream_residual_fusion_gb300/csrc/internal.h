@@ -59,4 +59,30 @@ cudaError_t launch_hc_post(const void* X, const void* F, const float* post, cons
 cudaError_t launch_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int d,
                           cudaStream_t stream);
 
+// Address ranges of the tensors of a call, for the overlap checks of the entry points.
+struct Span {
+  uintptr_t lo, hi;
+  bool empty() const { return hi <= lo; }
+};
+inline Span span(const void* p, uint64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Span{a, a + static_cast<uintptr_t>(bytes)};
+}
+inline bool overlap(Span a, Span b) { return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi; }
+
+// Outputs must not overlap inputs or each other; output `same_out` may be exactly equal (same
+// start and size) to input `same_in` (an in-place update).
+template <int NO, int NI>
+inline bool aliasing_ok(const Span (&outs)[NO], const Span (&ins)[NI], int same_out = -1, int same_in = -1) {
+  for (int i = 0; i < NO; ++i) {
+    for (int j = 0; j < NI; ++j) {
+      if (i == same_out && j == same_in && outs[i].lo == ins[j].lo && outs[i].hi == ins[j].hi) continue;
+      if (overlap(outs[i], ins[j])) return false;
+    }
+    for (int j = i + 1; j < NO; ++j)
+      if (overlap(outs[i], outs[j])) return false;
+  }
+  return true;
+}
+
 }  // namespace mhc

@@ -5,8 +5,8 @@ PyTorch is used for device memory and streams. If the library is missing or fail
 import of the binding raises; there is no other code path.
 
 Calls mirror the C ABI in include/mhc.h (same names without the `mhc_` prefix). Tensors must be
-CUDA, contiguous, with the dtypes the header lists; outputs are allocated here with torch unless
-passed in.
+CUDA (fused_step_host: per-token tensors on the host), contiguous, with the dtypes the header
+lists; outputs are allocated here with torch unless passed in.
 """
 from __future__ import annotations
 
@@ -58,6 +58,8 @@ SIGNATURES = {
     "mhc_step_scratch_bytes": (_SZ, [_I, _I]),
     "mhc_fused_step_noalloc": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P]),
     "mhc_noalloc_scratch_bytes": (_SZ, []),
+    "mhc_fused_step_host": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _I64, _P]),
+    "mhc_host_staging_bytes": (_SZ, [_I, _I, _I64, _I]),
     "mhc_mixes": (_I, [_P] * 8 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_sinkhorn": (_I, [_P] * 6 + [_I64, _I, _I, _F, _P]),
     "mhc_rmsnorm": (_I, [_P] * 3 + [_I64, _I, _F, _P]),
@@ -103,9 +105,9 @@ def _check(rc: int, where: str):
         raise MhcError(rc, where)
 
 
-def _need(t, dtype, name):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+def _need(t, dtype, name, device="cuda"):
+    if not isinstance(t, torch.Tensor) or t.device.type != device:
+        raise TypeError(f"{name} must be a {device} tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -145,14 +147,18 @@ def pack_weights(W, out=None, stream=None):
 def _step_outputs(X, out, with_mixes):
     N, n, d = X.shape
     dev = X.device
+    pin = dev.type == "cpu"                    # host outputs of fused_step_host: page-locked
     out = dict(out or {})
-    out.setdefault("Xp", torch.empty_like(X))
-    out.setdefault("y", torch.empty(N, d, dtype=torch.bfloat16, device=dev))
-    out.setdefault("pre", torch.empty(N, n, dtype=torch.float32, device=dev))
-    out.setdefault("post", torch.empty(N, n, dtype=torch.float32, device=dev))
-    out.setdefault("comb", torch.empty(N, n, n, dtype=torch.float32, device=dev))
+
+    def new(shape, dtype):
+        return torch.empty(shape, dtype=dtype, device=dev, pin_memory=pin)
+    out.setdefault("Xp", new(X.shape, torch.bfloat16))
+    out.setdefault("y", new((N, d), torch.bfloat16))
+    out.setdefault("pre", new((N, n), torch.float32))
+    out.setdefault("post", new((N, n), torch.float32))
+    out.setdefault("comb", new((N, n, n), torch.float32))
     if with_mixes:
-        out.setdefault("mixes", torch.empty(N, MIX, dtype=torch.float32, device=dev))
+        out.setdefault("mixes", new((N, MIX), torch.float32))
     return out
 
 
@@ -211,6 +217,43 @@ def fused_step_noalloc(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gai
         _ptr(o["comb"]), _ptr(o.get("mixes")), N, n, d, iters, hc_eps, norm_eps, flags,
         _stream(stream))
     _check(rc, "mhc_fused_step_noalloc")
+    return o
+
+
+def host_staging_bytes(d: int, chunk_tokens: int, with_mixes: bool = False,
+                       n: int = N_STREAMS) -> int:
+    return int(lib.mhc_host_staging_bytes(n, d, chunk_tokens, int(with_mixes)))
+
+
+def default_chunk_tokens(N: int) -> int:
+    """About 16 chunks, a multiple of 128 tokens, between 1024 and 8192 (N if smaller)."""
+    return max(1, min(N, max(1024, min(8192, -(-N // 16 // 128) * 128))))
+
+
+def fused_step_host(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, iters=20,
+                    hc_eps=1e-6, norm_eps=1e-6, flags=0, with_mixes=False, out=None,
+                    staging=None, chunk_tokens=None, stream=None):
+    """mhc_fused_step_host: the fused step on HOST tensors (X, F, pre/post/comb_prev and the
+    outputs on the CPU, pinned for overlap), parameters W, scale, base, gain on the GPU. The
+    outputs are complete once `stream` has been synchronised."""
+    _need(X, torch.bfloat16, "X", "cpu")
+    _need(F, torch.bfloat16, "F", "cpu")
+    for t, nm in ((pre_prev, "pre_prev"), (post_prev, "post_prev"), (comb_prev, "comb_prev")):
+        _need(t, torch.float32, nm, "cpu")
+    for t, nm in ((W, "W"), (scale, "scale"), (base, "base"), (gain, "gain")):
+        _need(t, torch.float32, nm)
+    N, n, d = X.shape
+    chunk = int(chunk_tokens or default_chunk_tokens(N))
+    o = _step_outputs(X, out, with_mixes)
+    if staging is None:
+        staging = torch.empty(host_staging_bytes(d, chunk, with_mixes, n), dtype=torch.uint8,
+                              device=W.device)
+    rc = lib.mhc_fused_step_host(
+        _ptr(X), _ptr(F), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev), _ptr(W), _ptr(scale),
+        _ptr(base), _ptr(gain), _ptr(o["Xp"]), _ptr(o["y"]), _ptr(o["pre"]), _ptr(o["post"]),
+        _ptr(o["comb"]), _ptr(o.get("mixes")), N, n, d, iters, hc_eps, norm_eps, flags,
+        _ptr(staging), staging.numel(), chunk, _stream(stream))
+    _check(rc, "mhc_fused_step_host")
     return o
 
 

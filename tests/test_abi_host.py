@@ -125,3 +125,38 @@ def test_other_calls_validation(M):
     assert lib.mhc_pack_weights(p[0], p[1], 4, 8, None) == M.MHC_ERR_SHAPE
     assert lib.mhc_mixes(*p[:8], 10, 4, 5120, 20, 1e-6, 1e-6, 0, None, 0, None) == M.MHC_ERR_WORKSPACE
     assert lib.mhc_mixes(*p[:8], 0, 4, 5120, 20, 1e-6, 1e-6, 0, p[7], 1 << 30, None) == M.MHC_OK
+
+
+def _host(M, N=256, n=4, d=5120, iters=20, flags=0, ptrs=None, staging=None, nbytes=1 << 40,
+          chunk=128):
+    p = [_addr(i) for i in range(15)] if ptrs is None else ptrs
+    st = _addr(20) if staging is None else staging
+    return M.lib.mhc_fused_step_host(*p, N, n, d, iters, 1e-6, 1e-6, flags, st, nbytes, chunk,
+                                     None)
+
+
+def test_host_pipeline_validation(M):
+    lib = M.lib
+    assert _host(M, chunk=0) == M.MHC_ERR_SHAPE
+    assert _host(M, n=3) == M.MHC_ERR_SHAPE
+    assert _host(M, N=-1) == M.MHC_ERR_SHAPE
+    assert _host(M, d=5000) == M.MHC_ERR_SHAPE           # the device step's shape rules
+    assert _host(M, iters=0) == M.MHC_ERR_SHAPE
+    assert _host(M, N=0) == M.MHC_OK
+    p = [_addr(i) for i in range(15)]
+    p[5] = None                                          # W_mix
+    assert _host(M, ptrs=p) == M.MHC_ERR_NULL
+    p = [_addr(i) for i in range(15)]
+    p[10] = ctypes.c_void_p(p[1].value + 4096)           # host y_out inside host F
+    assert _host(M, ptrs=p) == M.MHC_ERR_ALIAS
+    p = [_addr(i) for i in range(15)]
+    p[14] = ctypes.c_void_p(p[13].value + 64)            # mixes_out over comb_out
+    assert _host(M, ptrs=p) == M.MHC_ERR_ALIAS
+    assert _host(M, staging=ctypes.c_void_p(0)) == M.MHC_ERR_WORKSPACE
+    need = lib.mhc_host_staging_bytes(4, 5120, 128, 1)
+    assert need > 0 and lib.mhc_host_staging_bytes(4, 5120, 0, 1) == 0
+    assert lib.mhc_host_staging_bytes(4, 5120, 128, 0) < need
+    assert _host(M, nbytes=need - 1) == M.MHC_ERR_WORKSPACE
+    assert _host(M, staging=ctypes.c_void_p(A + 16)) == M.MHC_ERR_ALIGN
+    # two staging slots of 128 tokens, each at least the tokens' inputs and outputs
+    assert need >= M.lib.mhc_workspace_bytes(4, 5120) + 2 * 128 * (2 * 51200 + 2 * 96 + 96)

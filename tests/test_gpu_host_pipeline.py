@@ -1,0 +1,100 @@
+"""The fused step on host-resident tensors (mhc_fused_step_host): chunks through two staging
+slots on three streams give, token for token, the device step's results and the oracle's, for
+ragged last chunks, chunk sizes that are not a multiple of the token tile, one chunk larger than
+the batch, an in-place host update, and a caller stream other than the default."""
+import numpy as np
+import pytest
+import torch
+
+from tests.parity import check_step, oracle_step
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+HOST_KEYS = ("X", "F", "pre", "post", "comb")
+
+
+@pytest.fixture(scope="module")
+def M():
+    from stream_residual_fusion_gb300 import build
+    build.build()
+    import stream_residual_fusion_gb300.mhc as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def synth():
+    from stream_residual_fusion_gb300 import synth as s
+    return s
+
+
+def _host_inputs(inp):
+    return {k: inp[k].cpu().pin_memory() for k in HOST_KEYS}
+
+
+def _host_step(M, inp, h, stream=None, **kw):
+    o = M.fused_step_host(h["X"], h["F"], h["pre"], h["post"], h["comb"], inp["W"], inp["scale"],
+                          inp["base"], inp["gain"], stream=stream, **kw)
+    (stream or torch.cuda.current_stream()).synchronize()
+    return o
+
+
+def _device_step(M, inp, with_mixes):
+    o = M.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], inp["W"],
+                     inp["scale"], inp["base"], inp["gain"], with_mixes=with_mixes)
+    torch.cuda.synchronize()
+    return {k: v.cpu() for k, v in o.items()}
+
+
+@pytest.mark.parametrize("N,d,chunk,with_mixes", [
+    (700, 5120, 256, True),      # 3 chunks, last one 188 tokens
+    (1000, 512, 300, False),     # chunks that straddle token tiles
+    (90, 1024, 4096, True),      # one chunk larger than the batch
+    (1, 256, 1, True),           # one token
+])
+def test_host_pipeline_matches_device_step(M, synth, N, d, chunk, with_mixes):
+    inp = synth.make_inputs(N, 4, d, seed=7100 + N, device=DEV)
+    h = _host_inputs(inp)
+    got = _host_step(M, inp, h, chunk_tokens=chunk, with_mixes=with_mixes)
+    assert M.get_status() == M.MHC_OK
+    want = _device_step(M, inp, with_mixes)
+    assert set(got) == set(want)
+    for k in want:
+        assert got[k].device.type == "cpu"
+        assert torch.equal(got[k], want[k]), k
+
+
+def test_host_pipeline_oracle_parity_side_stream(M, synth):
+    N, d = 530, 5120
+    inp = synth.make_inputs(N, 4, d, seed=7200, device=DEV, scale_uniform=True, x_stream_std=True)
+    h = _host_inputs(inp)
+    side = torch.cuda.Stream()
+    got = _host_step(M, inp, h, stream=side, chunk_tokens=128, with_mixes=True)
+    check_step(got, oracle_step({k: v.cpu() for k, v in inp.items()}))
+
+
+def test_host_pipeline_in_place(M, synth):
+    N, d = 600, 2048
+    inp = synth.make_inputs(N, 4, d, seed=7300, device=DEV)
+    h = _host_inputs(inp)
+    want = _device_step(M, inp, False)
+    X_host = h["X"]
+    got = _host_step(M, inp, h, chunk_tokens=200, out={"Xp": X_host})
+    assert got["Xp"].data_ptr() == X_host.data_ptr()
+    for k in want:
+        assert torch.equal(got[k], want[k]), k
+
+
+def test_host_pipeline_repeated_calls_reuse_staging(M, synth):
+    N, d = 400, 1024
+    stg = torch.empty(M.host_staging_bytes(d, 128), dtype=torch.uint8, device=DEV)
+    for seed in (7400, 7401):
+        inp = synth.make_inputs(N, 4, d, seed=seed, device=DEV)
+        h = _host_inputs(inp)
+        got = _host_step(M, inp, h, chunk_tokens=128, staging=stg)
+        want = _device_step(M, inp, False)
+        for k in want:
+            assert torch.equal(got[k], want[k]), (seed, k)
+    with pytest.raises(M.MhcError):
+        M.fused_step_host(h["X"], h["F"], h["pre"], h["post"], h["comb"], inp["W"], inp["scale"],
+                          inp["base"], inp["gain"], chunk_tokens=256, staging=stg)
+    np.testing.assert_equal(M.get_status(), M.MHC_OK)
