@@ -8,12 +8,14 @@
  * Conventions for every call
  *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous, row-major, with
  *     the token axis flattened (N = B*T). bf16 tensors are passed as void*. The library never
- *     frees or keeps them.
+ *     frees or keeps them. (mhc_fused_step_host takes its per-token tensors as HOST pointers.)
  *   - Every pointer must be 16-byte aligned (MHC_ERR_ALIGN otherwise).
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy default
  *     stream). The library never synchronises, except in mhc_get_status.
  *   - The library allocates no device memory. Calls that need scratch take a caller-owned
  *     `workspace` of at least the size the matching *_workspace_bytes() call returns.
+ *     (mhc_fused_step_host creates three streams and a few events per device on its first call
+ *     there and keeps them until the process exits.)
  *   - Arguments are validated on the host before anything is launched; a negative return code
  *     means nothing was launched (except MHC_ERR_CUDA, which reports a launch failure).
  *   - Only n = 4 streams is built (the shape of the pages' block; (2+n)n = 24 mix numbers).
@@ -143,8 +145,8 @@ size_t mhc_noalloc_scratch_bytes(void);
 /* ---- the fused step on host-resident streams -------------------------------------------------
  * No counterpart in the paper (its step runs on device tensors): the same step as
  * mhc_fused_step for a caller whose per-token tensors are in HOST memory. The tokens are cut
- * into chunks of chunk_tokens; chunk i is copied into device staging slot i%2, stepped, and
- * copied back, on three internal streams of the current device, so that the host->device copy
+ * into chunks (see mhc_host_chunks); chunk i is copied into device staging slot i%3, stepped,
+ * and copied back, on three internal streams of the current device, so that the host->device copy
  * of chunk i+1, the step on chunk i and the device->host copy of chunk i-1 overlap. The
  * internal streams start after the work already queued on `stream`, and `stream` continues only
  * after the last output has reached the host: synchronise `stream` before reading the outputs
@@ -157,7 +159,7 @@ size_t mhc_noalloc_scratch_bytes(void);
  *   W_mix, scale, base, gain   DEVICE pointers (parameters stay resident on the GPU).
  *   staging: >= mhc_host_staging_bytes(n, d, chunk_tokens, mixes_out != NULL) device bytes,
  *        256-byte aligned (MHC_ERR_ALIGN otherwise): the workspace of mhc_fused_step followed by
- *        two slots of chunk_tokens tokens' inputs and outputs.
+ *        three slots of chunk_tokens tokens' inputs and outputs.
  * The internal streams and events are shared by all calls on a device: calls that overlap in
  * time -- from different threads, or on different caller streams -- must be serialised.
  * Returns MHC_OK or a negative code (as mhc_fused_step; MHC_ERR_SHAPE also for chunk_tokens
@@ -171,6 +173,14 @@ int mhc_fused_step_host(const void* X, const void* F, const float* pre_prev,
                         size_t staging_bytes, int64_t chunk_tokens, void* stream);
 /* Device bytes of the staging buffer of mhc_fused_step_host; 0 for an invalid shape or chunk. */
 size_t mhc_host_staging_bytes(int n, int d, int64_t chunk_tokens, int with_mixes);
+/* The chunks mhc_fused_step_host cuts N tokens into, in order: writes the first min(count,
+ * max_chunks) token counts to `counts` (may be NULL) and returns the count, or MHC_ERR_SHAPE for
+ * N < 0 or chunk_tokens < 1. When N >= 2(c/8 + c/4 + c/2) + c (c = chunk_tokens, c >= 8), the
+ * first three chunks are c/8, c/4, c/2 tokens and the last three c/2, c/4, c/8, so that the
+ * copy-in before the first step and the copy-out after the last, which overlap nothing, stay
+ * short; the chunks between hold c tokens, the last of them the remainder. Otherwise every chunk
+ * holds c tokens but the last.                                                                */
+int64_t mhc_host_chunks(int64_t N, int64_t chunk_tokens, int64_t* counts, int64_t max_chunks);
 
 /* ---- hc_mixes alone ------------------------------------------------------------------------
  * Stream weights for the feed-forward, Code: hc_mixes (+ the hc_split_sinkhorn kernel): from

@@ -1,4 +1,4 @@
-// host_pipeline.cu -- the fused step on host-resident tensors: token chunks flow through two
+// host_pipeline.cu -- the fused step on host-resident tensors: token chunks flow through three
 // device staging slots so that host->device copies, the fused kernel and device->host copies of
 // consecutive chunks overlap (three internal streams joined to the caller's stream by events).
 #include <cuda_runtime.h>
@@ -13,11 +13,15 @@ namespace mhc {
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Staging slots. With two, the copy-in of chunk i would wait for the copy-out of chunk i-2, which
+// trails the copy-in of chunk i-1 by one step kernel: a bubble per chunk. Three leave a chunk of
+// slack.
+constexpr int kSlots = 3;
 
 struct Lanes {
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
-  cudaEvent_t in_ready[2] = {}, computed[2] = {}, out_done[2] = {};
+  cudaEvent_t in_ready[kSlots] = {}, computed[kSlots] = {}, out_done[kSlots] = {};
   bool ok = false;
 };
 Lanes g_lanes[kMaxDevices];
@@ -35,7 +39,7 @@ Lanes* lanes() {
                 cudaStreamCreateWithFlags(&L.d2h, cudaStreamNonBlocking) == cudaSuccess &&
                 cudaEventCreateWithFlags(&L.start, cudaEventDisableTiming) == cudaSuccess &&
                 cudaEventCreateWithFlags(&L.done, cudaEventDisableTiming) == cudaSuccess;
-    for (int b = 0; good && b < 2; ++b)
+    for (int b = 0; good && b < kSlots; ++b)
       good = cudaEventCreateWithFlags(&L.in_ready[b], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&L.computed[b], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&L.out_done[b], cudaEventDisableTiming) == cudaSuccess;
@@ -70,6 +74,44 @@ SlotLayout slot_layout(int64_t chunk, int d, bool with_mixes) {
   return s;
 }
 
+// Token count of chunk i. The first and the last chunks ramp (c/8, c/4, c/2) so that the
+// copy-in before the first step and the copy-out after the last one, which overlap nothing, are
+// short; the rest are c tokens, the last full-size one taking the remainder. Batches under
+// 2(c/8 + c/4 + c/2) + c tokens use plain chunks of c.
+struct ChunkPlan {
+  int64_t N, c, ramp[3] = {}, ramp_sum = 0;
+  bool ramped = false;
+  ChunkPlan(int64_t n_tok, int64_t chunk) : N(n_tok), c(chunk) {
+    for (int k = 0; k < 3; ++k) {
+      ramp[k] = chunk >> (3 - k);
+      ramp_sum += ramp[k];
+    }
+    ramped = ramp[0] >= 1 && N >= 2 * ramp_sum + c;
+  }
+  // Calls f(start, count) for every chunk in order.
+  template <class Fn>
+  int each(Fn&& f) const {
+    int64_t t = 0;
+    int rc = 0;
+    if (!ramped) {
+      for (; t < N && rc == 0; t += c) rc = f(t, N - t < c ? N - t : c);
+      return rc;
+    }
+    for (int k = 0; k < 3 && rc == 0; ++k) {
+      rc = f(t, ramp[k]);
+      t += ramp[k];
+    }
+    const int64_t mid_end = N - ramp_sum;
+    for (; t < mid_end && rc == 0; t += c) rc = f(t, mid_end - t < c ? mid_end - t : c);
+    t = mid_end;
+    for (int k = 2; k >= 0 && rc == 0; --k) {
+      rc = f(t, ramp[k]);
+      t += ramp[k];
+    }
+    return rc;
+  }
+};
+
 }  // namespace
 }  // namespace mhc
 
@@ -80,7 +122,18 @@ extern "C" {
 size_t mhc_host_staging_bytes(int n, int d, int64_t chunk_tokens, int with_mixes) {
   const size_t ws = mhc_workspace_bytes(n, d);
   if (ws == 0 || chunk_tokens <= 0) return 0;
-  return a256(ws) + 2 * slot_layout(chunk_tokens, d, with_mixes != 0).bytes;
+  return a256(ws) + kSlots * slot_layout(chunk_tokens, d, with_mixes != 0).bytes;
+}
+
+int64_t mhc_host_chunks(int64_t N, int64_t chunk_tokens, int64_t* counts, int64_t max_chunks) {
+  if (N < 0 || chunk_tokens <= 0) return MHC_ERR_SHAPE;
+  int64_t k = 0;
+  ChunkPlan(N, chunk_tokens).each([&](int64_t, int64_t c) -> int {
+    if (counts != nullptr && k < max_chunks) counts[k] = c;
+    ++k;
+    return MHC_OK;
+  });
+  return k;
 }
 
 int mhc_fused_step_host(const void* X, const void* F, const float* pre_prev,
@@ -122,7 +175,8 @@ int mhc_fused_step_host(const void* X, const void* F, const float* pre_prev,
   const size_t packed = a256(mhc_packed_weights_bytes(n, d));
   uint8_t* ws = base_ptr;
   const SlotLayout lay = slot_layout(chunk_tokens, d, with_mixes);
-  uint8_t* slot[2] = {base_ptr + ws_bytes, base_ptr + ws_bytes + lay.bytes};
+  uint8_t* slot[kSlots];
+  for (int b = 0; b < kSlots; ++b) slot[b] = base_ptr + ws_bytes + b * lay.bytes;
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
 
   auto ck = [](cudaError_t e) { return e == cudaSuccess; };
@@ -139,13 +193,13 @@ int mhc_fused_step_host(const void* X, const void* F, const float* pre_prev,
   uint8_t* hy = static_cast<uint8_t*>(y_out);
   const size_t rowX = static_cast<size_t>(4) * d * 2, rowF = static_cast<size_t>(d) * 2;
   int64_t i = 0;
-  for (int64_t t0 = 0; t0 < N; t0 += chunk_tokens, ++i) {
-    const int b = static_cast<int>(i & 1);
-    const int64_t c = (N - t0) < chunk_tokens ? (N - t0) : chunk_tokens;
+  rc = ChunkPlan(N, chunk_tokens).each([&](int64_t t0, int64_t c) -> int {
+    const int b = static_cast<int>(i % kSlots);
     const size_t cc = static_cast<size_t>(c), tt = static_cast<size_t>(t0);
     uint8_t* S = slot[b];
-    // inputs of chunk i into slot b once chunk i-2 has left it
-    if (i >= 2 && !ck(cudaStreamWaitEvent(L->h2d, L->out_done[b], 0))) return MHC_ERR_CUDA;
+    // inputs of chunk i into slot b once chunk i-kSlots has left it
+    if (i >= kSlots && !ck(cudaStreamWaitEvent(L->h2d, L->out_done[b], 0))) return MHC_ERR_CUDA;
+    ++i;
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
     if (!ck(cudaMemcpyAsync(S + lay.X, hX + tt * rowX, cc * rowX, h2d, L->h2d)) ||
         !ck(cudaMemcpyAsync(S + lay.F, hF + tt * rowF, cc * rowF, h2d, L->h2d)) ||
@@ -156,16 +210,14 @@ int mhc_fused_step_host(const void* X, const void* F, const float* pre_prev,
       return MHC_ERR_CUDA;
     // the step on slot b
     if (!ck(cudaStreamWaitEvent(L->comp, L->in_ready[b], 0))) return MHC_ERR_CUDA;
-    rc = mhc_fused_step_packed(S + lay.X, S + lay.F, reinterpret_cast<float*>(S + lay.pre),
-                               reinterpret_cast<float*>(S + lay.post),
-                               reinterpret_cast<float*>(S + lay.comb), ws, scale, base, gain,
-                               S + lay.Xo, S + lay.y, reinterpret_cast<float*>(S + lay.po),
-                               reinterpret_cast<float*>(S + lay.uo),
-                               reinterpret_cast<float*>(S + lay.co),
-                               with_mixes ? reinterpret_cast<float*>(S + lay.mo) : nullptr, c, n,
-                               d, sinkhorn_iters, hc_eps, norm_eps, flags, ws + packed,
-                               ws_bytes - packed, L->comp);
-    if (rc != MHC_OK) return rc;
+    const int r = mhc_fused_step_packed(
+        S + lay.X, S + lay.F, reinterpret_cast<float*>(S + lay.pre),
+        reinterpret_cast<float*>(S + lay.post), reinterpret_cast<float*>(S + lay.comb), ws, scale,
+        base, gain, S + lay.Xo, S + lay.y, reinterpret_cast<float*>(S + lay.po),
+        reinterpret_cast<float*>(S + lay.uo), reinterpret_cast<float*>(S + lay.co),
+        with_mixes ? reinterpret_cast<float*>(S + lay.mo) : nullptr, c, n, d, sinkhorn_iters,
+        hc_eps, norm_eps, flags, ws + packed, ws_bytes - packed, L->comp);
+    if (r != MHC_OK) return r;
     if (!ck(cudaEventRecord(L->computed[b], L->comp))) return MHC_ERR_CUDA;
     // outputs of chunk i back to the host
     if (!ck(cudaStreamWaitEvent(L->d2h, L->computed[b], 0)) ||
@@ -177,7 +229,9 @@ int mhc_fused_step_host(const void* X, const void* F, const float* pre_prev,
         (with_mixes && !ck(cudaMemcpyAsync(mixes_out + tt * 24, S + lay.mo, cc * 96, d2h, L->d2h))) ||
         !ck(cudaEventRecord(L->out_done[b], L->d2h)))
       return MHC_ERR_CUDA;
-  }
+    return MHC_OK;
+  });
+  if (rc != MHC_OK) return rc;
   // join: the caller's stream continues once the last outputs are on the host
   if (!ck(cudaEventRecord(L->done, L->d2h)) || !ck(cudaStreamWaitEvent(caller, L->done, 0)))
     return MHC_ERR_CUDA;

@@ -60,6 +60,7 @@ SIGNATURES = {
     "mhc_noalloc_scratch_bytes": (_SZ, []),
     "mhc_fused_step_host": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _I64, _P]),
     "mhc_host_staging_bytes": (_SZ, [_I, _I, _I64, _I]),
+    "mhc_host_chunks": (_I64, [_I64, _I64, ctypes.POINTER(_I64), _I64]),
     "mhc_mixes": (_I, [_P] * 8 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_sinkhorn": (_I, [_P] * 6 + [_I64, _I, _I, _F, _P]),
     "mhc_rmsnorm": (_I, [_P] * 3 + [_I64, _I, _F, _P]),
@@ -223,6 +224,16 @@ def fused_step_noalloc(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gai
 def host_staging_bytes(d: int, chunk_tokens: int, with_mixes: bool = False,
                        n: int = N_STREAMS) -> int:
     return int(lib.mhc_host_staging_bytes(n, d, chunk_tokens, int(with_mixes)))
+
+
+def host_chunks(N: int, chunk_tokens: int) -> list[int]:
+    """Token counts of the chunks fused_step_host cuts N tokens into."""
+    k = int(lib.mhc_host_chunks(N, chunk_tokens, None, 0))
+    if k < 0:
+        raise MhcError(k, "mhc_host_chunks")
+    buf = (_I64 * max(k, 1))()
+    lib.mhc_host_chunks(N, chunk_tokens, buf, k)
+    return list(buf[:k])
 
 
 def default_chunk_tokens(N: int) -> int:

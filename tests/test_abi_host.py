@@ -158,5 +158,32 @@ def test_host_pipeline_validation(M):
     assert lib.mhc_host_staging_bytes(4, 5120, 128, 0) < need
     assert _host(M, nbytes=need - 1) == M.MHC_ERR_WORKSPACE
     assert _host(M, staging=ctypes.c_void_p(A + 16)) == M.MHC_ERR_ALIGN
-    # two staging slots of 128 tokens, each at least the tokens' inputs and outputs
-    assert need >= M.lib.mhc_workspace_bytes(4, 5120) + 2 * 128 * (2 * 51200 + 2 * 96 + 96)
+    # three staging slots of 128 tokens, each at least the tokens' inputs and outputs
+    assert need >= M.lib.mhc_workspace_bytes(4, 5120) + 3 * 128 * (2 * 51200 + 2 * 96 + 96)
+
+
+def _chunks_by_definition(N, c):
+    """The chunk rule as the header states it, written out."""
+    r = [c // 8, c // 4, c // 2]
+    if c >= 8 and N >= 2 * sum(r) + c:
+        mid = N - 2 * sum(r)
+        return r + [c] * (mid // c) + ([mid % c] if mid % c else []) + r[::-1]
+    return [c] * (N // c) + ([N % c] if N % c else [])
+
+
+def test_host_chunk_plan(M):
+    assert M.lib.mhc_host_chunks(-1, 8, None, 0) == M.MHC_ERR_SHAPE
+    assert M.lib.mhc_host_chunks(10, 0, None, 0) == M.MHC_ERR_SHAPE
+    assert M.host_chunks(0, 128) == []
+    assert M.host_chunks(1500, 256) == [32, 64, 128, 256, 256, 256, 256, 28, 128, 64, 32]
+    assert M.host_chunks(703, 256) == [256, 256, 191]
+    assert M.host_chunks(704, 256) == [32, 64, 128, 256, 128, 64, 32]
+    for N in list(range(0, 300)) + [4095, 4096, 32768, 131072, 10**9 + 7]:
+        for c in (1, 2, 7, 8, 9, 100, 128, 2048):
+            if N // c > 5000:
+                continue
+            got = M.host_chunks(N, c)
+            assert got == _chunks_by_definition(N, c), (N, c)
+            assert sum(got) == N and all(1 <= x <= c for x in got)
+    buf = (ctypes.c_int64 * 2)()
+    assert M.lib.mhc_host_chunks(1500, 256, buf, 2) == 11 and list(buf) == [32, 64]

@@ -50,6 +50,8 @@ def _device_step(M, inp, with_mixes):
     (1000, 512, 300, False),     # chunks that straddle token tiles
     (90, 1024, 4096, True),      # one chunk larger than the batch
     (1, 256, 1, True),           # one token
+    (1500, 1024, 256, True),     # ramped: 32, 64, 128, 4 x 256 + 28, 128, 64, 32 tokens
+    (704, 512, 256, False),      # the smallest batch that ramps: one full-size chunk
 ])
 def test_host_pipeline_matches_device_step(M, synth, N, d, chunk, with_mixes):
     inp = synth.make_inputs(N, 4, d, seed=7100 + N, device=DEV)
