@@ -353,6 +353,7 @@ def run_ours(args):
                    "step": "mhc_pack_weights + mhc_fused_step_packed"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "frac_of_nominal_8000": achieved / 8000.0,
                      "kernel": "step_kernel<true> (fused)",
                      "kernel_ms_avg": fused_avg, "kernel_ms_p50": statistics.median(fused_ms),
                      "kernel_ms_p95": sorted(fused_ms)[int(0.95 * (len(fused_ms) - 1))],
@@ -375,6 +376,108 @@ def run_ours(args):
     return 0
 
 
+# bytes per token each kernel of the unfused form must move (d = 5120, n = 4, no m output)
+UNFUSED_BYTES_PER_TOKEN = {
+    "hc_post": 4 * 5120 * 2 + 5120 * 2 + 16 + 64 + 4 * 5120 * 2,   # read X, F, u, C; write X'
+    "mixes": 4 * 5120 * 2 + 96,                                      # read X'; write p, u, C
+    "hc_pre": 4 * 5120 * 2 + 16 + 5120 * 2,                          # read X', p; write y_hat
+    "rmsnorm": 5120 * 2 + 5120 * 2,                                  # read y_hat; write y
+}
+
+
+def run_unfused(args):
+    """The unfused GPU form of the same step: hc_post, hc_mixes (+ split and Sinkhorn), hc_pre and
+    RMSNorm as four launches that pass X' and y_hat through HBM, timed per kernel beside the fused
+    step on the same inputs (one GPU)."""
+    import torch
+    from stream_residual_fusion_gb300 import mhc, synth
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    N, d = w.N, w.d
+    inp = synth.make_workload(w, seed=3000, device=dev)
+    inp.pop("outliers", None)
+    stream = torch.cuda.current_stream(dev)
+    Xp = torch.empty_like(inp["X"])
+    yhat = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(yhat)
+    mx = {"pre": torch.empty(N, 4, device=dev), "post": torch.empty(N, 4, device=dev),
+          "comb": torch.empty(N, 4, 4, device=dev)}
+    ws = torch.empty(mhc.workspace_bytes(d), dtype=torch.uint8, device=dev)
+    out = {"Xp": torch.empty_like(inp["X"]), "y": torch.empty_like(yhat),
+           "pre": torch.empty(N, 4, device=dev), "post": torch.empty(N, 4, device=dev),
+           "comb": torch.empty(N, 4, 4, device=dev)}
+    Wp = torch.empty(mhc.packed_weights_bytes(d), dtype=torch.uint8, device=dev)
+    scratch = torch.empty(mhc.step_scratch_bytes(d), dtype=torch.uint8, device=dev)
+    names = list(UNFUSED_BYTES_PER_TOKEN)
+
+    def unfused(ev=None):
+        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        rec(0)
+        mhc.hc_post(inp["X"], inp["F"], inp["post"], inp["comb"], out=Xp, stream=stream)
+        rec(1)
+        mhc.mixes(Xp, inp["W"], inp["scale"], inp["base"], with_mixes=False, workspace=ws,
+                  out=mx, stream=stream)
+        rec(2)
+        mhc.hc_pre(Xp, inp["pre"], out=yhat, stream=stream)
+        rec(3)
+        mhc.rmsnorm(yhat, inp["gain"], 1e-6, out=y, stream=stream)
+        rec(4)
+
+    def fused(ev=None):
+        mhc.pack_weights(inp["W"], out=Wp, stream=stream)
+        if ev:
+            ev[0].record(stream)
+        mhc.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None,
+                       inp["scale"], inp["base"], inp["gain"], W_packed=Wp, scratch=scratch,
+                       out=out, stream=stream)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        unfused()
+        fused()
+    torch.cuda.synchronize()
+    K = args.steps
+    T = lambda: torch.cuda.Event(enable_timing=True)
+    evu = [[T() for _ in range(5)] for _ in range(K)]
+    evf = [[T() for _ in range(2)] for _ in range(K)]
+    for i in range(K):                      # interleaved, so both see the same clocks
+        unfused(evu[i])
+        fused(evf[i])
+    torch.cuda.synchronize()
+    if mhc.get_status() != mhc.MHC_OK:
+        raise RuntimeError("device-side wait gave up")
+    same = bool(torch.equal(Xp, out["Xp"]))
+    per = {nm: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evu)
+           for j, nm in enumerate(names)}
+    total = statistics.median(e[0].elapsed_time(e[4]) for e in evu)
+    fused_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evf)
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    kernels = {}
+    for nm in names:
+        b = N * UNFUSED_BYTES_PER_TOKEN[nm]
+        kernels[nm] = {"ms_p50": per[nm], "algorithmic_bytes": b,
+                       "gbs": b / (per[nm] / 1e3) / 1e9, "frac": b / (per[nm] / 1e3) / 1e9 / peak}
+    unf_bytes = N * sum(UNFUSED_BYTES_PER_TOKEN.values())
+    line = {
+        "metric": "unfused four-kernel mHC step tokens/s at n=4,d=5120 (beside the fused step)",
+        "form": "unfused", "value": N / (total / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": K, "warmup": args.warmup, "ms_per_step": total, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} (N={N}), n=4, d={d}", "sinkhorn_iters": 20},
+        "kernels": kernels,
+        "unfused_algorithmic_bytes_per_token": sum(UNFUSED_BYTES_PER_TOKEN.values()),
+        "fused_algorithmic_bytes_per_token": STREAM_BYTES_PER_TOKEN + SMALL_BYTES_PER_TOKEN,
+        "unfused_ms_p50": total, "fused_ms_p50": fused_ms, "fused_speedup": total / fused_ms,
+        "unfused_bytes_per_launch_sum": unf_bytes, "peak_gbs": peak, "peak_kind": peak_kind,
+        "x_prime_identical": same, "gpu_launches": K * 6,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -383,11 +486,15 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--form", choices=("fused", "unfused"), default="fused",
+                    help="unfused: time the four-kernel form beside the fused step (one GPU)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="synthetic workload (default: the B=4,T=8192 prefill; others are for profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.form == "unfused":
+        return run_unfused(args)
     return run_ours(args)
 
 

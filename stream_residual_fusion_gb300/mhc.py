@@ -269,18 +269,19 @@ def fused_step_host(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, 
 
 
 def mixes(X, W, scale, base, *, iters=20, hc_eps=1e-6, norm_eps=1e-6, flags=0, with_mixes=True,
-          workspace=None, stream=None):
+          workspace=None, out=None, stream=None):
     """hc_mixes alone (mhc_mixes). Returns dict with pre, post, comb (and mixes)."""
     _need(X, torch.bfloat16, "X")
     for t, nm in ((W, "W"), (scale, "scale"), (base, "base")):
         _need(t, torch.float32, nm)
     N, n, d = X.shape
     dev = X.device
-    o = {"pre": torch.empty(N, n, dtype=torch.float32, device=dev),
-         "post": torch.empty(N, n, dtype=torch.float32, device=dev),
-         "comb": torch.empty(N, n, n, dtype=torch.float32, device=dev)}
+    o = dict(out or {})
+    o.setdefault("pre", torch.empty(N, n, dtype=torch.float32, device=dev))
+    o.setdefault("post", torch.empty(N, n, dtype=torch.float32, device=dev))
+    o.setdefault("comb", torch.empty(N, n, n, dtype=torch.float32, device=dev))
     if with_mixes:
-        o["mixes"] = torch.empty(N, MIX, dtype=torch.float32, device=dev)
+        o.setdefault("mixes", torch.empty(N, MIX, dtype=torch.float32, device=dev))
     if workspace is None:
         workspace = torch.empty(workspace_bytes(d, n), dtype=torch.uint8, device=dev)
     rc = lib.mhc_mixes(_ptr(X), _ptr(W), _ptr(scale), _ptr(base), _ptr(o.get("mixes")),
