@@ -53,6 +53,11 @@ extern "C" {
  * them (a group of co-resident CTAs). 0 = automatic (the fewest that fit on chip).            */
 #define MHC_SPLIT_SHIFT          8
 #define MHC_SPLIT_MASK           (0xFu << MHC_SPLIT_SHIFT)
+/* Bits 16..20: tokens per tile of the step kernel / 8 (1..16, i.e. 8..128 tokens; larger values
+ * are MHC_ERR_SHAPE). 0 = automatic: the height that minimises the busiest group's share of the
+ * tiles (plus a fixed cost per tile), so the last round of tiles keeps every group busy.       */
+#define MHC_TILE_SHIFT           16
+#define MHC_TILE_MASK            (0x1Fu << MHC_TILE_SHIFT)
 
 /* ---- sizes ------------------------------------------------------------------------------- */
 /* Bytes of the packed projection weights (3 bf16 planes of W_mix plus padding, in the layout
@@ -234,6 +239,9 @@ int mhc_get_status(void* stream);
 /* Launch shape of the fused step on the current device: the width split it uses for (n, d,
  * flags) and how many groups of `split` CTAs the device holds at once. Diagnostic; needs a GPU. */
 int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* groups);
+/* Tokens per tile the fused step uses for N tokens of width d with `flags` on the current device
+ * (see MHC_TILE_SHIFT), or a negative code. Diagnostic; needs a GPU.                          */
+int mhc_step_tile(int64_t N, int n, int d, unsigned flags);
 /* Phase tracing of the fused step (off by default). With a device buffer set, every later
  * launch whose grid fits records, per CTA, 8 uint64 values from the GPU's nanosecond timer:
  * the start time, then nanoseconds since the start at: loads issued, main loop done, partials

@@ -54,6 +54,7 @@ int check_step_shape(int64_t N, int n, int d, int iters, unsigned flags, int* sp
   if (n != 4 || N < 0 || N > kMaxTokens || iters < 1 || d <= 0) return MHC_ERR_SHAPE;
   const int forced = static_cast<int>((flags & MHC_SPLIT_MASK) >> MHC_SPLIT_SHIFT);
   *split = choose_split(d, forced);
+  if (tile_flag(flags) < 0) return MHC_ERR_SHAPE;
   return *split == 0 ? MHC_ERR_SHAPE : MHC_OK;
 }
 
@@ -139,8 +140,8 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
 extern "C" {
 
 size_t mhc_packed_weights_bytes(int n, int d) {
-  if (n != 4 || d <= 0 || d % STEP_DC != 0) return 0;
-  return static_cast<size_t>(d / STEP_DC) * STEP_WBLOCK_BYTES;
+  if (n != 4 || d <= 0 || d % STEP_WDC != 0) return 0;
+  return static_cast<size_t>(d / STEP_WDC) * STEP_WBLOCK_BYTES;
 }
 
 size_t mhc_step_scratch_bytes(int n, int d) {
@@ -154,11 +155,11 @@ size_t mhc_workspace_bytes(int n, int d) {
   return align256(packed) + step_scratch_bytes();
 }
 
-int mhc_packed_block_columns(void) { return STEP_DC; }
+int mhc_packed_block_columns(void) { return STEP_WDC; }
 
 int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* stream) {
   if (!W_mix || !W_packed) return MHC_ERR_NULL;
-  if (n != 4 || d <= 0 || d % STEP_DC != 0) return MHC_ERR_SHAPE;
+  if (n != 4 || d <= 0 || d % STEP_WDC != 0) return MHC_ERR_SHAPE;
   if (!aligned16(W_mix) || !aligned16(W_packed)) return MHC_ERR_ALIGN;
   const uint64_t K = 4ull * d;
   if (overlap(span(W_mix, 96 * K), span(W_packed, mhc_packed_weights_bytes(4, d)))) return MHC_ERR_ALIAS;
@@ -338,6 +339,14 @@ int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters) 
   if (rc != MHC_OK) return rc;
   *split = sp;
   return cuda_code(step_occupancy(sp, clusters));
+}
+
+int mhc_step_tile(int64_t N, int n, int d, unsigned flags) {
+  int sp = 0, groups = 0;
+  const int rc = check_step_shape(N, n, d, 1, flags, &sp);
+  if (rc != MHC_OK) return rc;
+  if (step_occupancy(sp, &groups) != cudaSuccess || groups < 1) return MHC_ERR_CUDA;
+  return choose_tile(N, groups, tile_flag(flags));
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -9,21 +9,22 @@
 // tiles persistently (tile c, c + #groups, ...). The launch is cooperative with one CTA per SM,
 // so every CTA of a group is resident and the groups use all SMs:
 //   * Each CTA owns d/split columns of every stream (d = 5120: 8 CTAs x 640 columns). The CTAs'
-//     columns interleave in steps of STEP_DC, so at every stage the group reads one contiguous
-//     run of STEP_DC*split columns of each token row.
-//   * Warp 0 drives a TMA ring: per stage [128 tokens x STEP_DC] tiles of X_0..X_3 and F (tensor
-//     copies) and the stage's block of packed projection weights (one contiguous bulk copy: the
-//     weights are packed as the exact shared-memory image the tensor cores read).
+//     columns interleave in slots of STEP_DC columns, so at every slot the group reads one
+//     contiguous run of STEP_DC*split columns of each token row.
+//   * Warp 0 drives the X/F ring: per slot, [128 tokens x STEP_DC] tiles of X_0..X_3 and F
+//     (tensor copies). The packed projection weights (32-column blocks, packed as the exact
+//     shared-memory image the tensor cores read) flow through a ring of their own that the MMA
+//     thread refills, so weight traffic never holds up the stream loads.
 //   * 8 consumer warps (2 threads per token) compute hc_post in place in shared memory, its sum
 //     of squares, hc_pre and its sum of squares; y_hat goes to a TMEM stash. While doing so they
 //     normalise the previous tile's y_hat from the same stash slot into the F tile they just
-//     read, so the previous tile's y leaves with this stage's stores.
+//     read, so the previous tile's y leaves with this slot's stores.
 //   * Warp 1 issues tcgen05.mma: D[128 tokens x 80] += X'[128 x 16] * Wp[80 x 16]^T per stream
-//     and K-step. Accumulation groups of 16 MMAs alternate between two TMEM accumulators; the
+//     and K-step. Accumulation groups of 16 MMAs alternate between two TMEM accumulators and the
 //     consumers fold each finished group into float32 running sums in shared memory.
-//   * Warp 10 stores X' and y with TMA straight from the stage's tiles and frees the stage as
-//     soon as the stores have read it.
-//   * After a tile's last stage the consumers post their slice's partial sums to the group
+//   * Warp 10 stores X' and y with TMA straight from the slot's tiles and frees the slot as soon
+//     as the stores have read it.
+//   * After a tile's last slot the consumers post their slice's partial sums to the group
 //     through a scratch area in global memory (L2) and release-ordered counters; warp 11
 //     finishes the tile's mix numbers (scale, split, Sinkhorn) while the consumers move on.
 #include <cuda.h>
@@ -42,47 +43,57 @@ namespace mhc {
 namespace {
 
 constexpr int TT = STEP_TT;
-constexpr int DC = STEP_DC;
+constexpr int DC = STEP_DC;             // columns per X/F slot (128-byte rows)
 constexpr int ROWB = STEP_ROW_BYTES;
-constexpr int CPT = STEP_CHUNKS / 2;    // 16-byte chunks per consumer thread per stage
-constexpr int KSTEPS = DC / 16;         // MMA K-steps per stream per stage
-constexpr int NSTAGE = DC == 16 ? 6 : 3;            // TMA ring depth
+constexpr int WDC = STEP_WDC;           // columns per packed weight block: half a slot
+constexpr int HALVES = DC / WDC;        // weight blocks, and consumer passes, per slot
+constexpr int CPH = 2;                  // 16-byte chunks per consumer thread per pass
+constexpr int KSTEPS = WDC / 16;        // MMA K-steps per stream per weight block
+constexpr int PG = 16 / (4 * HALVES * KSTEPS);      // slots per accumulation group (16 MMAs)
+constexpr int NSTAGE = DC == 32 ? 4 : 2;            // X/F ring depth (40 or 80 KB slots)
+constexpr int NW = 2;                   // weight ring entries (one block each)
+// slots by which the y_hat stash ring outlasts a tile: the previous tile's RMS factor is taken
+// after slot RLAG - 1 and used from slot RLAG on
+constexpr int RLAG = DC == 32 ? 2 : 1;
 constexpr int NCONS = 8;                // consumer warps (2 per TMEM lane quarter)
 constexpr int NROLE = 2;                // warp 0: TMA producer; warp 1: TMEM owner and MMA issuer
 constexpr int STORE_WARP = NROLE + NCONS;           // warp 10: X'/y TMA stores
 constexpr int FIN_WARP = STORE_WARP + 1;            // warp 11: scale, split, Sinkhorn
 constexpr int NTHREADS = (FIN_WARP + 1) * 32;
-constexpr int PG = 16 / (4 * KSTEPS);   // stages per accumulation group (16 MMAs)
-static_assert((PG & (PG - 1)) == 0, "PG is a power of two");
-constexpr int TILE_BYTES = TT * ROWB;
-constexpr int STAGE_BYTES = 5 * TILE_BYTES + STEP_WBLOCK_BYTES;
-constexpr int PART_STRIDE = 28;                   // floats per token row of the running sums
+static_assert(2 * HALVES * CPH == STEP_CHUNKS, "2 thread halves x passes x chunks cover a row");
+static_assert(4 * HALVES * KSTEPS * PG == 16, "accumulation groups of 16 MMAs");
+constexpr int TILE_BYTES = TT * ROWB;               // one [128 tokens x DC] tile: 16 KB
+constexpr int STAGE_BYTES = 5 * TILE_BYTES;         // X_0..X_3 and F
+constexpr int RUN_STRIDE = 24;                      // floats per token of the local running sums
+constexpr int PART_STRIDE = 28;                     // floats per token of an exchange row
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = STEP_MMA_N;         // two accumulators, at columns 0 and 80
 constexpr uint32_t STASH_COL = 2 * ACC_COLS;
-// y_hat stash: a ring of S + 2 stage slots per thread half (see the consumers), so the widest
-// slice is (352 columns / (2 halves * 4*CPT columns) - 2) stages.
-constexpr int STASH_SLOTS = static_cast<int>(TMEM_COLS - STASH_COL) / (2 * 4 * CPT);
-constexpr int MAX_SLICE = (STASH_SLOTS - 2) * DC;       // 640 columns for DC = 32
+// y_hat stash: a ring of S + RLAG slots of SLOT_COLS columns (both thread halves), so the
+// widest slice is STASH_SLOTS - RLAG slots.
+constexpr int PASS_COLS = 4 * CPH;                   // packed bf16 pairs per thread and pass
+constexpr int SLOT_COLS = 2 * HALVES * PASS_COLS;    // 32
+constexpr int STASH_SLOTS = static_cast<int>(TMEM_COLS - STASH_COL) / SLOT_COLS;
+constexpr int MAX_SLICE = (STASH_SLOTS - RLAG) * DC;    // 640 columns
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
 constexpr uint64_t DEBUG_WAIT_NS = 2000000ull;           // 2 ms
 
-constexpr int PART_BYTES = TT * PART_STRIDE * 4;   // one tile's running sums; two of them
-constexpr int OFF_PART = NSTAGE * STAGE_BYTES;
-constexpr int OFF_RY = OFF_PART + 2 * PART_BYTES;
-constexpr int OFF_BARS = OFF_RY + TT * 4;
-constexpr int NBARS = 3 * NSTAGE + 4;   // full/empty/xready per stage; accready[2]; drained; never
+constexpr int PART_BYTES = TT * PART_STRIDE * 4;   // one tile's exchange rows (global scratch)
+constexpr int RUN_BYTES = TT * RUN_STRIDE * 4;     // one tile's running sums; two of them
+constexpr int OFF_W = NSTAGE * STAGE_BYTES;
+constexpr int OFF_PART = OFF_W + NW * STEP_WBLOCK_BYTES;
+constexpr int OFF_BARS = OFF_PART + 2 * RUN_BYTES;
+// full/empty/xready per X/F slot; wfull/wempty per weight entry; accready[2]; drained; never
+constexpr int NBARS = 3 * NSTAGE + 2 * NW + 4;
 constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;   // + slack for 1 KB alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
-static_assert(PG >= 2, "a group is folded one stage into the next group");
-static_assert(CPT == 1 || CPT == 2, "one or two 16-byte chunks per consumer thread");
+static_assert(STAGE_BYTES % 1024 == 0 && STEP_WBLOCK_BYTES % 1024 == 0, "tile alignment");
 
 __host__ __device__ constexpr int xtile(int b, int k) { return b * STAGE_BYTES + k * TILE_BYTES; }
 __host__ __device__ constexpr int ftile(int b) { return b * STAGE_BYTES + 4 * TILE_BYTES; }
-__host__ __device__ constexpr int wtile(int b, int k) {
-  return b * STAGE_BYTES + 5 * TILE_BYTES + k * STEP_WSTREAM_BYTES;
+__host__ __device__ constexpr int wtile(int e, int k) {
+  return OFF_W + e * STEP_WBLOCK_BYTES + k * STEP_WSTREAM_BYTES;
 }
 // y staging at the very end reuses the X/F tiles of the idle ring: slot j -> stage j/5, tile j%5.
 __host__ __device__ constexpr int yslot(int j) { return (j / 5) * STAGE_BYTES + (j % 5) * TILE_BYTES; }
@@ -105,6 +116,7 @@ struct StepParams {
   unsigned* counters;          // per group: syready[2], pready[2], pfree[2] (zeroed per launch)
   float* gpart;                // per group: [2 buffers][split ranks][TT tokens][PART_STRIDE]
   int N;
+  int tt;                      // tokens per tile (a multiple of 8, <= TT); rows >= tt are idle
   int d;
   int split;
   int slice;
@@ -154,29 +166,12 @@ __device__ __forceinline__ uint4 rms_scale8(const uint32_t* w, const float* __re
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ __forceinline__ void stash_load(uint32_t taddr, uint32_t (&w)[4 * CPT]) {
-  if constexpr (CPT == 1) {
-    uint32_t (&v)[4] = *reinterpret_cast<uint32_t(*)[4]>(w);
-    tmem_ld_x4(taddr, v);
-  } else {
-    uint32_t (&v)[8] = *reinterpret_cast<uint32_t(*)[8]>(w);
-    tmem_ld_x8(taddr, v);
-  }
+// One pass's y_hat (PASS_COLS packed bf16 pairs) to or from the TMEM stash.
+__device__ __forceinline__ void stash_load(uint32_t taddr, uint32_t (&w)[PASS_COLS]) { tmem_ld_x8(taddr, w); }
+__device__ __forceinline__ void stash_load_nowait(uint32_t taddr, uint32_t (&w)[PASS_COLS]) {
+  tmem_ld_x8_nowait(taddr, w);
 }
-__device__ __forceinline__ void stash_load_nowait(uint32_t taddr, uint32_t (&w)[4 * CPT]) {
-  if constexpr (CPT == 1) {
-    tmem_ld_x4_nowait(taddr, *reinterpret_cast<uint32_t(*)[4]>(w));
-  } else {
-    tmem_ld_x8_nowait(taddr, *reinterpret_cast<uint32_t(*)[8]>(w));
-  }
-}
-__device__ __forceinline__ void stash_store(uint32_t taddr, const uint32_t (&w)[4 * CPT]) {
-  if constexpr (CPT == 1) {
-    tmem_st_x4(taddr, w[0], w[1], w[2], w[3]);
-  } else {
-    tmem_st_x8(taddr, *reinterpret_cast<const uint32_t(*)[8]>(w));
-  }
-}
+__device__ __forceinline__ void stash_store(uint32_t taddr, const uint32_t (&w)[PASS_COLS]) { tmem_st_x8(taddr, w); }
 
 // Persistent: group c of gridDim.x / split groups handles tiles c, c + #groups, ... The TMA ring,
 // the accumulation groups and the barrier phases run on across tiles.
@@ -191,17 +186,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
   uint64_t* empty = full + NSTAGE;
   uint64_t* xready = empty + NSTAGE;
-  uint64_t* accready = xready + NSTAGE;     // [2]: an accumulation group finished in buffer i
+  uint64_t* wfull = xready + NSTAGE;        // [NW]: the block in weight entry e has landed
+  uint64_t* wempty = wfull + NW;            // [NW]: the MMAs that read weight entry e are done
+  uint64_t* accready = wempty + NW;         // [2]: an accumulation group finished in buffer i
   uint64_t* drained = accready + 2;         // the last X'/y stores have left the ring
   uint64_t* never = drained + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
-  float* ry = reinterpret_cast<float*>(sm + OFF_RY);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int split = P.split;
   const uint32_t g = blockIdx.x % split;              // rank within the group
-  const int ntiles = (P.N + TT - 1) / TT;
+  const int tt = P.tt;
+  const int ntiles = (P.N + tt - 1) / tt;
   const int nclust = gridDim.x / split;               // groups
   const int c0 = blockIdx.x / split;                  // this CTA's group = its first tile
   // group exchange (global memory): counters and the partial sums of every rank
@@ -212,10 +209,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return P.gpart + ((static_cast<size_t>(c0) * 2 + pb) * split + rank) * (TT * PART_STRIDE);
   };
   const int col0 = static_cast<int>(g) * DC;          // first column of this CTA's slice
-  const int cstride = DC * split;                     // stride between its stages' columns
-  const int S = P.nsteps;
-  const int G = (S + PG - 1) / PG;                    // accumulation groups per tile
-  const int R = S + 2;                                // y_hat stash ring slots
+  const int cstride = DC * split;                     // stride between its slots' columns
+  const int S = P.nsteps;                             // slots per tile
+  const int G = S / PG;                               // accumulation groups per tile
+  const int R = S + RLAG;                             // y_hat stash ring slots
   const int d = P.d;
   bool timed_out = false;
   auto limit = [&]() { return timed_out ? 0ull : WAIT_LIMIT_NS; };
@@ -232,6 +229,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&full[b], 1);
       mbar_init(&empty[b], FUSED ? 2 : 1 + NCONS);
       mbar_init(&xready[b], NCONS);
+    }
+    for (int e = 0; e < NW; ++e) {
+      mbar_init(&wfull[e], 1);
+      mbar_init(&wempty[e], 1);
     }
     mbar_init(&accready[0], 1);
     mbar_init(&accready[1], 1);
@@ -258,11 +259,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_prefetch_desc(&tm_y);
       }
       const uint64_t stream_pol = policy_evict_first();
-      const uint64_t weight_pol = policy_evict_last();
-      const uint32_t bytes = 4 * TILE_BYTES + (FUSED ? TILE_BYTES : 0) + STEP_WBLOCK_BYTES;
+      const uint32_t bytes = (FUSED ? 5u : 4u) * static_cast<uint32_t>(tt * ROWB);   // tt-row boxes
       int gs = 0;
       for (int tile = c0; tile < ntiles; tile += nclust) {
-        const int t0 = tile * TT;
+        const int t0 = tile * tt;
         for (int s = 0; s < S; ++s, ++gs) {
           const int b = gs % NSTAGE;
           if (gs >= NSTAGE) {
@@ -274,37 +274,67 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int k = 0; k < 4; ++k)
             tma_load_3d_hint(sm + xtile(b, k), &tm_x, &full[b], i0, k, t0, stream_pol);
           if (FUSED) tma_load_2d_hint(sm + ftile(b), &tm_f, &full[b], i0, t0, stream_pol);
-          bulk_load_hint(sm + wtile(b, 0), P.w_packed + static_cast<size_t>(i0 / DC) * STEP_WBLOCK_BYTES,
-                         STEP_WBLOCK_BYTES, &full[b], weight_pol);
         }
         if (auto tr = trace_rec(tile)) tr[1] = global_timer_ns();
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // It also runs the weight ring, whose only reader it is: global weight block u (block
+    // u % HALVES of slot u / HALVES) goes to entry u % NW, and an entry is refilled with block
+    // u + NW once the MMAs that read block u have completed. The X/F producer never waits on it.
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(TT, STEP_MMA_N);
-      int gs = 0, it = 0;
-      for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
+      const uint64_t weight_pol = policy_evict_last();
+      const int nblocks = ((ntiles - c0 + nclust - 1) / nclust) * S * HALVES;
+      auto load_block = [&](int u) {
+        const int e = u % NW;
+        const int slot_in_tile = (u / HALVES) % S;
+        const int blk = (col0 + slot_in_tile * cstride) / WDC + u % HALVES;
+        mbar_arrive_expect_tx(&wfull[e], STEP_WBLOCK_BYTES);
+        bulk_load_hint(sm + wtile(e, 0), P.w_packed + static_cast<size_t>(blk) * STEP_WBLOCK_BYTES,
+                       STEP_WBLOCK_BYTES, &wfull[e], weight_pol);
+      };
+      for (int u = 0; u < NW && u < nblocks; ++u) load_block(u);
+      int gs = 0;
+      for (int tile = c0; tile < ntiles; tile += nclust) {
         for (int s = 0; s < S; ++s, ++gs) {
           const int b = gs % NSTAGE;
           if (!mbar_wait(FUSED ? &xready[b] : &full[b], (gs / NSTAGE) & 1, limit())) timed_out = true;
           tc_fence_after();
-          const int gg = gs / PG;           // slices hold whole groups: gs % PG == s % PG
+          // accumulation groups of PG slots alternate between the two accumulators; slices hold
+          // whole groups, so gs % PG == s % PG
+          const int gg = gs / PG;
           const uint32_t acc = tmem + static_cast<uint32_t>((gg & 1) * ACC_COLS);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t a0 = smem_u32(sm + xtile(b, k));
-            const uint32_t b0 = smem_u32(sm + wtile(b, k));
+          for (int j = 0; j < HALVES; ++j) {
+            const int u = gs * HALVES + j, e = u % NW;
+            if (!mbar_wait(&wfull[e], (u / NW) & 1, limit())) timed_out = true;
+            tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-              umma_bf16(acc, sdesc_kmajor_swizzled(a0 + 32 * kk, ROWB),
-                        sdesc_kmajor_swizzled(b0 + 32 * kk, ROWB), idesc,
-                        (s % PG != 0 || k != 0 || kk != 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t a0 = smem_u32(sm + xtile(b, k));
+              const uint32_t b0 = smem_u32(sm + wtile(e, k));
+#pragma unroll
+              for (int kk = 0; kk < KSTEPS; ++kk) {
+                umma_bf16(acc, sdesc_kmajor_swizzled(a0 + 32 * (j * KSTEPS + kk), ROWB),
+                          sdesc_kmajor_swizzled(b0 + 32 * kk, STEP_WROW_BYTES), idesc,
+                          (s % PG != 0 || j != 0 || k != 0 || kk != 0) ? 1u : 0u);
+              }
             }
+            umma_commit(&wempty[e]);
           }
           umma_commit(&empty[b]);
           if (s % PG == PG - 1 || s == S - 1) umma_commit(&accready[gg & 1]);
+          // refill this slot's weight entries with the blocks NW ahead once its MMAs are done
+#pragma unroll
+          for (int j = 0; j < HALVES; ++j) {
+            const int u = gs * HALVES + j;
+            if (u + NW < nblocks) {
+              if (!mbar_wait(&wempty[u % NW], (u / NW) & 1, limit())) timed_out = true;
+              load_block(u + NW);
+            }
+          }
         }
       }
     }
@@ -313,8 +343,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (FUSED && lane == 0) {
       const uint64_t stream_pol = policy_evict_first();
       int gs = 0;
-      for (int tile = c0, it = 0; tile < ntiles; tile += nclust, ++it) {
-        const int t0 = tile * TT;
+      for (int tile = c0; tile < ntiles; tile += nclust) {
+        const int t0 = tile * tt;
         for (int s = 0; s < S; ++s, ++gs) {
           const int b = gs % NSTAGE;
           if (!mbar_wait(&xready[b], (gs / NSTAGE) & 1, limit())) timed_out = true;
@@ -322,13 +352,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) tma_store_3d_hint(&tm_xo, sm + xtile(b, k), i0, k, t0, stream_pol);
           if (gs >= R) {
-            // the y the consumers normalised into the F tile: global stage gs - R
+            // the y the consumers normalised into the F tile: global slot gs - R
             const int src = gs - R;
             const int ytile = c0 + (src / S) * nclust;
-            tma_store_2d_hint(&tm_y, sm + ftile(b), col0 + (src % S) * cstride, ytile * TT, stream_pol);
+            tma_store_2d_hint(&tm_y, sm + ftile(b), col0 + (src % S) * cstride, ytile * tt, stream_pol);
           }
           bulk_commit();
-          bulk_wait_read<0>();          // the stage's tiles have been read: free the stage
+          bulk_wait_read<0>();          // the slot's tiles have been read: free the slot
           mbar_arrive(&empty[b]);
         }
       }
@@ -338,20 +368,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------------ consumers
     const int c = warp - NROLE;
     const int sub = warp & 3;           // TMEM lane quarter this warp may access
-    const int h = c >> 2;               // which half of a stage's columns, which 12 mix numbers
+    const int h = c >> 2;               // which half of a slot's columns, which 12 mix numbers
     const int tl = sub * 32 + lane;     // token row within a tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
-    uint32_t row_off[CPT];
+    // pass hs of this thread covers 16-byte chunks chunk0(hs) + q, q < CPH, of its token row
+    auto chunk0 = [&](int hs) { return (h * HALVES + hs) * CPH; };
+    uint32_t row_off[HALVES][CPH];
 #pragma unroll
-    for (int q = 0; q < CPT; ++q) row_off[q] = tile_chunk_offset(tl, h * CPT + q);
-    // the y_hat stash: a ring of R slots of 4*CPT columns; global stage gs uses slot gs % R
-    const uint32_t stash = lane_base + STASH_COL + static_cast<uint32_t>(h * R * 4 * CPT);
-    auto slot_addr = [&](int slot) { return stash + static_cast<uint32_t>(slot * 4 * CPT); };
+    for (int hs = 0; hs < HALVES; ++hs)
+#pragma unroll
+      for (int q = 0; q < CPH; ++q) row_off[hs][q] = tile_chunk_offset(tl, chunk0(hs) + q);
+    // the y_hat stash: a ring of R slots; global slot gs uses ring slot gs % R, pass hs of this
+    // thread half its PASS_COLS columns at hs * PASS_COLS
+    const uint32_t stash = lane_base + STASH_COL + static_cast<uint32_t>(h * R * HALVES * PASS_COLS);
+    auto slot_addr = [&](int slot, int hs) {
+      return stash + static_cast<uint32_t>((slot * HALVES + hs) * PASS_COLS);
+    };
 
     f2 cu[4], cc[4][4], cp[4];
     auto load_coeffs = [&](int tile) {
-      const int token = tile * TT + tl;
-      const bool valid = FUSED && tile < ntiles && token < P.N;
+      const int token = tile * tt + tl;
+      const bool valid = FUSED && tile < ntiles && tl < tt && token < P.N;
       const bool row_dest = (P.flags & 1u) != 0;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -369,7 +406,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     };
     auto part_of = [&](int it_) {   // running sums of this thread for tile iteration it_
-      return reinterpret_cast<float*>(sm + OFF_PART + (it_ & 1) * PART_BYTES) + tl * PART_STRIDE;
+      return reinterpret_cast<float*>(sm + OFF_PART + (it_ & 1) * RUN_BYTES) + tl * RUN_STRIDE;
     };
     // RMS factor of tile iteration it_ for this token: y_hat sums of squares of every slice
     auto rms_factor = [&](int it_) {
@@ -389,8 +426,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float r = __frsqrt_rn(__fdiv_rn(sy, static_cast<float>(d)) + P.norm_eps);
       return f2{r, r};
     };
-    // fold accumulation group gg into its tile's running sums; after a tile's last group, post
-    // the tile's partials to the group
+    // fold accumulation group gg (global numbering) into its tile's running sums; after a
+    // tile's last group, post the tile's partials to the group
     auto fold = [&](int gg) {
       if (!mbar_wait(&accready[gg & 1], (gg >> 1) & 1, limit())) timed_out = true;
       tc_fence_after();
@@ -414,8 +451,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     load_coeffs(c0);
 
-    // RMS factors: r_old for tile it-2 (consumed in stages 0, 1), r_new for tile it-1 (from
-    // stage 2 on; computed there, two stages after the group posted it)
+    // RMS factors: r_old for tile it-2 (consumed in slots s < RLAG), r_new for tile it-1 (from
+    // slot RLAG on; computed after slot RLAG - 1)
     f2 r_old{0.f, 0.f}, r_new{0.f, 0.f};
     int gs = 0, it = 0, folded = 0;
     int slot = 0;                        // gs % R, kept incrementally
@@ -431,90 +468,97 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       f2 sx2{0.f, 0.f}, sy2{0.f, 0.f};
       for (int s = 0; s < S; ++s, ++gs) {
         const int b = gs % NSTAGE;
-        // the slot this stage writes holds the y_hat of global stage gs - R (tile it-1, or
-        // it-2 in stages 0 and 1): read it now, normalise it into the F tile once F has been
-        // read; the store warp writes it out with this stage's X'
+        // the ring slot this slot writes holds the y_hat of global slot gs - R (tile it-1, or
+        // it-2 in slots s < RLAG): read it now, normalise it into the F tile once F has been read; the
+        // store warp writes it out with this slot's X'
         const bool consume = FUSED && gs >= R;
-        uint32_t prev[4 * CPT];
-        if (consume) stash_load_nowait(slot_addr(slot), prev);
+        uint32_t prev[PASS_COLS];
+        if (consume) stash_load_nowait(slot_addr(slot, 0), prev);
         if (!mbar_wait(&full[b], (gs / NSTAGE) & 1, limit())) timed_out = true;
         if (consume) tmem_ld_wait();
-        f2 lx{0.f, 0.f};   // this stage's sum of squares, added to the running sum once
+        f2 lx{0.f, 0.f};   // this slot's sum of squares, added to the running sum once
         if (FUSED) {
-          uint32_t ywall[4 * CPT];
-          const f2 r_src = s >= 2 ? r_new : r_old;
-          const int ycol = col0 + (s >= 2 ? s - 2 : s + S - 2) * cstride;   // stage of gs - R
+          const f2 r_src = s >= RLAG ? r_new : r_old;
+          const int ycol = col0 + (s >= RLAG ? s - RLAG : s + S - RLAG) * cstride;   // slot of gs - R
           f2 ly{0.f, 0.f};
 #pragma unroll
-          for (int q = 0; q < CPT; ++q) {
-            uint32_t xw[4][4], fw[4];
+          for (int hs = 0; hs < HALVES; ++hs) {
+            if (consume && hs > 0) stash_load(slot_addr(slot, hs), prev);
+            uint32_t ywall[PASS_COLS];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[q]);
-              xw[k][0] = v.x;
-              xw[k][1] = v.y;
-              xw[k][2] = v.z;
-              xw[k][3] = v.w;
-            }
-            {
-              const uint4 v = *reinterpret_cast<const uint4*>(sm + ftile(b) + row_off[q]);
-              fw[0] = v.x;
-              fw[1] = v.y;
-              fw[2] = v.z;
-              fw[3] = v.w;
-            }
-            if (consume) {
-              *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[q]) =
-                  rms_scale8(prev + 4 * q, P.gain, ycol + (h * CPT + q) * 8, r_src);
-            }
-            uint32_t ow[4][4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const f2 f = bf2_to_f2(fw[w]);
-              f2 x[4], xp[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) x[j] = bf2_to_f2(xw[j][w]);
+            for (int q = 0; q < CPH; ++q) {
+              uint32_t xw[4][4], fw[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                // X'_k = fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0))))
-                f2 mixed = mul2(cc[0][k], x[0]);
-                mixed = fma2(cc[1][k], x[1], mixed);
-                mixed = fma2(cc[2][k], x[2], mixed);
-                mixed = fma2(cc[3][k], x[3], mixed);
-                ow[k][w] = f2_to_bf2(fma2(cu[k], f, mixed));
-                xp[k] = bf2_to_f2(ow[k][w]);
-                lx = fma2(xp[k], xp[k], lx);
+                const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[hs][q]);
+                xw[k][0] = v.x;
+                xw[k][1] = v.y;
+                xw[k][2] = v.z;
+                xw[k][3] = v.w;
               }
-              // y_hat = fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0)))
-              f2 yh = mul2(cp[0], xp[0]);
-              yh = fma2(cp[1], xp[1], yh);
-              yh = fma2(cp[2], xp[2], yh);
-              yh = fma2(cp[3], xp[3], yh);
-              ywall[4 * q + w] = f2_to_bf2(yh);
-              const f2 yr = bf2_to_f2(ywall[4 * q + w]);
-              ly = fma2(yr, yr, ly);
-            }
+              {
+                const uint4 v = *reinterpret_cast<const uint4*>(sm + ftile(b) + row_off[hs][q]);
+                fw[0] = v.x;
+                fw[1] = v.y;
+                fw[2] = v.z;
+                fw[3] = v.w;
+              }
+              if (consume) {
+                *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[hs][q]) =
+                    rms_scale8(prev + 4 * q, P.gain, ycol + (chunk0(hs) + q) * 8, r_src);
+              }
+              uint32_t ow[4][4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              *reinterpret_cast<uint4*>(sm + xtile(b, k) + row_off[q]) =
-                  make_uint4(ow[k][0], ow[k][1], ow[k][2], ow[k][3]);
+              for (int w = 0; w < 4; ++w) {
+                const f2 f = bf2_to_f2(fw[w]);
+                f2 x[4], xp[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = bf2_to_f2(xw[j][w]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  // X'_k = fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0))))
+                  f2 mixed = mul2(cc[0][k], x[0]);
+                  mixed = fma2(cc[1][k], x[1], mixed);
+                  mixed = fma2(cc[2][k], x[2], mixed);
+                  mixed = fma2(cc[3][k], x[3], mixed);
+                  ow[k][w] = f2_to_bf2(fma2(cu[k], f, mixed));
+                  xp[k] = bf2_to_f2(ow[k][w]);
+                  lx = fma2(xp[k], xp[k], lx);
+                }
+                // y_hat = fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0)))
+                f2 yh = mul2(cp[0], xp[0]);
+                yh = fma2(cp[1], xp[1], yh);
+                yh = fma2(cp[2], xp[2], yh);
+                yh = fma2(cp[3], xp[3], yh);
+                ywall[4 * q + w] = f2_to_bf2(yh);
+                const f2 yr = bf2_to_f2(ywall[4 * q + w]);
+                ly = fma2(yr, yr, ly);
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4*>(sm + xtile(b, k) + row_off[hs][q]) =
+                    make_uint4(ow[k][0], ow[k][1], ow[k][2], ow[k][3]);
+            }
+            stash_store(slot_addr(slot, hs), ywall);
           }
-          stash_store(slot_addr(slot), ywall);
           sy2 = add2(sy2, ly);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&xready[b]);
         } else {
 #pragma unroll
-          for (int q = 0; q < CPT; ++q) {
+          for (int hs = 0; hs < HALVES; ++hs) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[q]);
-              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            for (int q = 0; q < CPH; ++q) {
 #pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                const f2 x = bf2_to_f2(wv[w]);
-                lx = fma2(x, x, lx);
+              for (int k = 0; k < 4; ++k) {
+                const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[hs][q]);
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  const f2 x = bf2_to_f2(wv[w]);
+                  lx = fma2(x, x, lx);
+                }
               }
             }
           }
@@ -523,12 +567,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         sx2 = add2(sx2, lx);
         slot = slot + 1 == R ? 0 : slot + 1;
-        // Fold group q one stage into group q+1 (global numbering, across tiles): the MMA that
-        // reuses q's accumulator (group q+2) starts only after this warp's xready of a later stage.
-        if ((gs & (PG - 1)) == 1 && gs > PG) fold(folded++);
-        // the previous tile's RMS factor, needed from stage 2 on: fetched after stage 1's work is
-        // published, so the wait overlaps this stage's MMAs and stores
-        if (FUSED && s == 1 && it > 0) r_new = rms_factor(it - 1);
+        // Fold group q in the last slot of group q+1 (global numbering, across tiles): the MMA
+        // that reuses q's accumulator (group q+2) starts only after this warp's xready of a
+        // later slot.
+        if (gs % PG == PG - 1 && gs >= 2 * PG - 1) fold(folded++);
+        // the previous tile's RMS factor, needed from slot RLAG on: fetched after slot RLAG-1's
+        // work is published, so the wait overlaps that slot's MMAs and stores
+        if (FUSED && s == RLAG - 1 && it > 0) r_new = rms_factor(it - 1);
       }
       if (FUSED) tmem_wait_st();
       if (tr && warp == NROLE && lane == 0) tr[2] = global_timer_ns() - tr[0];
@@ -553,30 +598,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int ngroups_total = it * G;
     while (folded < ngroups_total) fold(folded++);
     if (FUSED && it > 0) {
-      // y still in the stash: the last R global stages (tile it-1's stages and, before them, the
-      // last two stages of tile it-2)
+      // y still in the stash: the last R global slots (tile it-1's slots and, before them, the
+      // last RLAG slots of tile it-2)
       const f2 r_last = rms_factor(it - 1);
-      const f2 r_before = r_new;    // tile it-2's factor (computed in tile it-1's stage 2)
+      const f2 r_before = r_new;    // tile it-2's factor (computed during tile it-1)
       if (!mbar_wait(drained, 0, limit())) timed_out = true;   // the ring is idle now
       const uint64_t stream_pol = policy_evict_first();
       const int first = std::max(0, gs - R);
       for (int g0 = first; g0 < gs; g0 += NYSLOTS) {
         const int g1 = std::min(gs, g0 + NYSLOTS);
         for (int src = g0; src < g1; ++src) {
-          uint32_t w[4 * CPT];
-          stash_load(slot_addr(src % R), w);
           const f2 r = (src / S == it - 1) ? r_last : r_before;
 #pragma unroll
-          for (int q = 0; q < CPT; ++q)
-            *reinterpret_cast<uint4*>(sm + yslot(src - g0) + row_off[q]) =
-                rms_scale8(w + 4 * q, P.gain, col0 + (src % S) * cstride + (h * CPT + q) * 8, r);
+          for (int hs = 0; hs < HALVES; ++hs) {
+            uint32_t w[PASS_COLS];
+            stash_load(slot_addr(src % R, hs), w);
+#pragma unroll
+            for (int q = 0; q < CPH; ++q)
+              *reinterpret_cast<uint4*>(sm + yslot(src - g0) + row_off[hs][q]) =
+                  rms_scale8(w + 4 * q, P.gain, col0 + (src % S) * cstride + (chunk0(hs) + q) * 8, r);
+          }
         }
         fence_proxy_async_smem();
         named_bar_sync(1, NCONS * 32);
         if (warp == NROLE && lane == 0) {
           for (int src = g0; src < g1; ++src) {
             const int ytile = c0 + (src / S) * nclust;
-            tma_store_2d_hint(&tm_y, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * TT, stream_pol);
+            tma_store_2d_hint(&tm_y, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, stream_pol);
           }
           bulk_commit();
           bulk_wait_read<0>();
@@ -590,13 +638,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // lane j owning comb row j, 8 tokens per pass.
     const int q = lane >> 2;
     const int j = lane & 3;
-    const int per = TT / split;
+    const int per = tt / split;
     int it = 0;
     for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
       const int pb = it & 1;
       if (!gwait(&pready[pb], static_cast<unsigned>(((it >> 1) + 1) * split * NCONS), limit()))
         timed_out = true;
-      const int t0 = tile * TT;
+      const int t0 = tile * tt;
       // 16 tokens per pass (two per lane group); after the last pass's reads the peers may
       // reuse their partials buffers
       for (int base_t = 0; base_t < per; base_t += 16) {
@@ -707,10 +755,10 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
-bool map_streams(CUtensorMap* m, const void* p, int64_t N, int d) {   // [N, 4, d]
+bool map_streams(CUtensorMap* m, const void* p, int64_t N, int d, uint32_t box_rows) {   // [N, 4, d]
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), 4, static_cast<cuuint64_t>(N)};
   const cuuint64_t str[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 8};
-  const cuuint32_t box[3] = {DC, 1, TT};
+  const cuuint32_t box[3] = {DC, 1, box_rows};
   return make_map(m, p, 3, dims, str, box);
 }
 bool map_rows(CUtensorMap* m, const void* p, int64_t rows, int64_t cols, uint32_t box_rows) {
@@ -743,15 +791,33 @@ cudaError_t resident_ctas(Kern kern, int* ctas) {
 }  // namespace
 
 int choose_split(int d, int forced) {
-  // slices of whole accumulation groups, at least 4 stages (the previous tile's RMS factor is
-  // taken at stage 2), and a stash ring of S + 2 slots that fits TMEM
+  // slices of whole accumulation groups, at least 128 columns (the previous tile's RMS factor
+  // is taken after slot RLAG - 1), and a stash ring of S + RLAG slots that fits TMEM
   auto ok = [d](int s) {
-    return d > 0 && d % (DC * PG * s) == 0 && d / s <= MAX_SLICE && d / s >= 4 * DC;
+    return d > 0 && d % (DC * PG * s) == 0 && d / s <= MAX_SLICE && d / s >= 4 * WDC;
   };
   if (forced != 0) return (forced == 1 || forced == 2 || forced == 4 || forced == 8) && ok(forced) ? forced : 0;
   for (int s : {1, 2, 4, 8})
     if (ok(s)) return s;
   return 0;
+}
+
+int choose_tile(int64_t N, int groups, int forced) {
+  if (forced != 0) return forced;
+  // the tile height that minimises the busiest group's work, ceil(tiles / groups) tiles of tt
+  // tokens each plus a fixed cost per tile; ties go to the taller tile
+  int best = TT;
+  int64_t best_cost = INT64_MAX;
+  for (int tt = TT; tt >= 8; tt -= 8) {
+    const int64_t tiles = (N + tt - 1) / tt;
+    const int64_t rounds = (tiles + groups - 1) / groups;
+    const int64_t cost = rounds * (tt + kTileCostTokens);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = tt;
+    }
+  }
+  return best;
 }
 
 size_t step_scratch_bytes() {
@@ -765,26 +831,27 @@ size_t step_scratch_bytes() {
 }
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
-  CUtensorMap tx, tf, txo, ty;
-  if (!map_streams(&tx, a.X, a.N, a.d)) return cudaErrorInvalidValue;
-  if (fused) {
-    if (!map_rows(&tf, a.F, a.N, a.d, TT)) return cudaErrorInvalidValue;
-    if (!map_streams(&txo, a.X_out, a.N, a.d)) return cudaErrorInvalidValue;
-    if (!map_rows(&ty, a.y_out, a.N, a.d, TT)) return cudaErrorInvalidValue;
-  } else {
-    tf = tx;
-    txo = tx;
-    ty = tx;
-  }
   auto kern = fused ? step_kernel<true> : step_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int ctas = 0;
   e = resident_ctas(kern, &ctas);
   if (e != cudaSuccess) return e;
-  const int tiles = static_cast<int>((a.N + TT - 1) / TT);
-  const int ngroups = std::max(1, std::min(tiles, ctas / a.split));
   if (ctas < a.split) return cudaErrorInvalidConfiguration;
+  const int tt = choose_tile(a.N, ctas / a.split, tile_flag(a.flags));
+  const int tiles = static_cast<int>((a.N + tt - 1) / tt);
+  const int ngroups = std::max(1, std::min(tiles, ctas / a.split));
+  CUtensorMap tx, tf, txo, ty;
+  if (!map_streams(&tx, a.X, a.N, a.d, tt)) return cudaErrorInvalidValue;
+  if (fused) {
+    if (!map_rows(&tf, a.F, a.N, a.d, tt)) return cudaErrorInvalidValue;
+    if (!map_streams(&txo, a.X_out, a.N, a.d, tt)) return cudaErrorInvalidValue;
+    if (!map_rows(&ty, a.y_out, a.N, a.d, tt)) return cudaErrorInvalidValue;
+  } else {
+    tf = tx;
+    txo = tx;
+    ty = tx;
+  }
 
   StepParams P{};
   P.pre_prev = a.pre_prev;
@@ -809,6 +876,7 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   if (counter_bytes + static_cast<size_t>(ngroups) * a.split * 2 * PART_BYTES > a.scratch_bytes)
     return cudaErrorInvalidValue;
   P.N = static_cast<int>(a.N);
+  P.tt = tt;
   P.d = a.d;
   P.split = a.split;
   P.slice = a.d / a.split;

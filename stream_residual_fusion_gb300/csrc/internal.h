@@ -42,6 +42,19 @@ struct StepArgs {
 // Returns the split (1, 2, 4 or 8) the step kernel uses for width d, or 0 if d is not supported.
 // `forced` = 0 picks automatically.
 int choose_split(int d, int forced);
+// Tokens per tile of the step kernel for N tokens on `groups` groups (a multiple of 8, <= 128);
+// `forced` != 0 is returned as is.
+int choose_tile(int64_t N, int groups, int forced);
+// The fixed cost of a tile, in tokens of streaming work, that choose_tile charges per tile.
+// Measured on GB300 at d = 5120: a tile of tt tokens takes about (tt + 96) tokens' worth of
+// time (every tile runs its 20 pipeline slots, each paying load latency), e.g. 685 us for 256
+// tiles of 128 tokens against 955 us for 512 tiles of 64.
+constexpr int kTileCostTokens = 96;
+// Tile height forced by the flags (MHC_TILE_SHIFT bits), 0 if automatic; -1 if invalid.
+inline int tile_flag(unsigned flags) {
+  const int v = static_cast<int>((flags >> 16) & 0x1Fu);
+  return v == 0 ? 0 : (v <= 16 ? 8 * v : -1);
+}
 constexpr int kMaxTokens = 65535 * 128;
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream);

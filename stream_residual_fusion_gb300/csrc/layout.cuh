@@ -1,6 +1,6 @@
-// layout.cuh -- geometry of the fused step's pipeline stages, shared by the fused kernel and the
+// layout.cuh -- geometry of the fused step's pipeline, shared by the fused kernel and the
 // weight-packing kernel (the packed weights are stored as the exact shared-memory image that the
-// fused kernel's tensor-core operand tiles need, so one contiguous bulk copy brings a stage's
+// fused kernel's tensor-core operand tiles need, so one contiguous bulk copy brings a block of
 // weights).
 #pragma once
 #include <cstdint>
@@ -8,21 +8,37 @@
 namespace mhc {
 
 constexpr int STEP_TT = 128;     // tokens per tile (the MMA's M)
-constexpr int STEP_DC = 32;      // columns of d per pipeline stage
-constexpr int STEP_ROW_BYTES = STEP_DC * 2;              // one bf16 tile row: 64 bytes
-constexpr int STEP_CHUNKS = STEP_ROW_BYTES / 16;         // 16-byte chunks per tile row
+
+// X and F slots: STEP_DC columns of d per pipeline slot (32: 64-byte rows, a 4-deep ring of
+// 40 KB slots; 64: 128-byte rows, a 2-deep ring of 80 KB slots).
+constexpr int STEP_DC = 32;
+constexpr int STEP_ROW_BYTES = STEP_DC * 2;
+constexpr int STEP_CHUNKS = STEP_ROW_BYTES / 16;         // 16-byte chunks per row
+
+// Packed weights: blocks of STEP_WDC columns of every stream, each the B operand of one half
+// of a slot's MMAs.
+constexpr int STEP_WDC = 32;
+constexpr int STEP_WROW_BYTES = STEP_WDC * 2;            // 64 bytes
+constexpr int STEP_WCHUNKS = STEP_WROW_BYTES / 16;
 constexpr int STEP_WROWS = 72;   // 3 bf16 planes x 24 mix rows
 constexpr int STEP_MMA_N = 80;   // the MMA's N: weight rows 72..79 are zero
-// one column block of the packed weights: 4 streams x [80 rows x DC columns]
-constexpr int STEP_WSTREAM_BYTES = STEP_MMA_N * STEP_ROW_BYTES;
+// one column block of the packed weights: 4 streams x [80 rows x STEP_WDC columns]
+constexpr int STEP_WSTREAM_BYTES = STEP_MMA_N * STEP_WROW_BYTES;
 constexpr int STEP_WBLOCK_BYTES = 4 * STEP_WSTREAM_BYTES;
 
-// Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile with STEP_DC
-// columns, stored with the hardware swizzle whose width is the row size (32, 64 or 128 bytes):
-// chunk c of row r sits at chunk c ^ ((r * row_bytes / 128) mod chunks_per_row).
+// Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile with `row_bytes`
+// per row (32, 64 or 128), stored with the hardware swizzle of that width: chunk c of row r sits
+// at chunk c ^ ((r * row_bytes / 128) mod chunks_per_row).
+__host__ __device__ constexpr uint32_t swizzled_chunk_offset(int row, int chunk, int row_bytes) {
+  return static_cast<uint32_t>(row * row_bytes +
+                               ((chunk ^ ((row * row_bytes >> 7) & (row_bytes / 16 - 1))) << 4));
+}
+// ... of an X/F tile (128-byte rows) and of a packed weight tile (64-byte rows)
 __host__ __device__ constexpr uint32_t tile_chunk_offset(int row, int chunk) {
-  return static_cast<uint32_t>(row * STEP_ROW_BYTES +
-                               ((chunk ^ ((row * STEP_ROW_BYTES >> 7) & (STEP_CHUNKS - 1))) << 4));
+  return swizzled_chunk_offset(row, chunk, STEP_ROW_BYTES);
+}
+__host__ __device__ constexpr uint32_t wtile_chunk_offset(int row, int chunk) {
+  return swizzled_chunk_offset(row, chunk, STEP_WROW_BYTES);
 }
 
 // Packed weight row of plane pl (0 hi, 1 mid, 2 lo) of mix row r: each half of the 24 mix rows

@@ -12,26 +12,26 @@ namespace {
 
 // Split W fp32 [24, 4d] into three bf16 planes, hi = bf16(w), mid = bf16(w - hi),
 // lo = bf16(w - hi - mid) (the differences are exact in fp32), and store them as the fused
-// kernel's shared-memory image: column block jb (STEP_DC columns of every stream) is
-// [4 streams][80 rows][STEP_DC columns] with plane pl of mix row r in row packed_row(r, pl),
+// kernel's shared-memory image: column block jb (STEP_WDC columns of every stream) is
+// [4 streams][80 rows][STEP_WDC columns] with plane pl of mix row r in row packed_row(r, pl),
 // rows 72..79 zero, and the 16-byte chunks of each row swizzled as the tensor cores read them.
 // One thread per 16-byte output chunk.
 __global__ void pack_kernel(const float* __restrict__ W, uint8_t* __restrict__ P, int d) {
   const int64_t K = 4 * static_cast<int64_t>(d);
-  const int64_t nblocks = d / STEP_DC;
-  const int64_t total = nblocks * 4 * STEP_MMA_N * STEP_CHUNKS;
+  const int64_t nblocks = d / STEP_WDC;
+  const int64_t total = nblocks * 4 * STEP_MMA_N * STEP_WCHUNKS;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int chunk = static_cast<int>(idx % STEP_CHUNKS);
-    const int row = static_cast<int>((idx / STEP_CHUNKS) % STEP_MMA_N);
-    const int k = static_cast<int>((idx / (STEP_CHUNKS * STEP_MMA_N)) % 4);
-    const int64_t jb = idx / (STEP_CHUNKS * STEP_MMA_N * 4);
+    const int chunk = static_cast<int>(idx % STEP_WCHUNKS);
+    const int row = static_cast<int>((idx / STEP_WCHUNKS) % STEP_MMA_N);
+    const int k = static_cast<int>((idx / (STEP_WCHUNKS * STEP_MMA_N)) % 4);
+    const int64_t jb = idx / (STEP_WCHUNKS * STEP_MMA_N * 4);
     uint32_t words[4] = {0u, 0u, 0u, 0u};
     if (row < STEP_WROWS) {
       const int half = row / 36, rem = row % 36;
       const int pl = rem / 12;
       const int r = 12 * half + rem % 12;
-      const int64_t col = k * static_cast<int64_t>(d) + jb * STEP_DC + chunk * 8;
+      const int64_t col = k * static_cast<int64_t>(d) + jb * STEP_WDC + chunk * 8;
       __nv_bfloat16 v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -48,7 +48,7 @@ __global__ void pack_kernel(const float* __restrict__ W, uint8_t* __restrict__ P
                    (static_cast<uint32_t>(__bfloat16_as_ushort(v[2 * e + 1])) << 16);
       }
     }
-    uint8_t* dst = P + jb * STEP_WBLOCK_BYTES + k * STEP_WSTREAM_BYTES + tile_chunk_offset(row, chunk);
+    uint8_t* dst = P + jb * STEP_WBLOCK_BYTES + k * STEP_WSTREAM_BYTES + wtile_chunk_offset(row, chunk);
     *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
   }
 }
@@ -225,7 +225,7 @@ int grid_for(int64_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_pack(const float* W, void* packed, int d, cudaStream_t stream) {
-  const int64_t chunks = static_cast<int64_t>(d / STEP_DC) * 4 * STEP_MMA_N * STEP_CHUNKS;
+  const int64_t chunks = static_cast<int64_t>(d / STEP_WDC) * 4 * STEP_MMA_N * STEP_WCHUNKS;
   pack_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(W, static_cast<uint8_t*>(packed), d);
   return cudaGetLastError();
 }

@@ -30,6 +30,7 @@ MHC_ERR_WORKSPACE = -7
 COMB_ROW_DEST = 0x1
 DEBUG_NEVER_ARRIVE = 0x2
 SPLIT_SHIFT = 8
+TILE_SHIFT = 16
 
 N_STREAMS = 4
 MIX = (2 + N_STREAMS) * N_STREAMS
@@ -71,6 +72,7 @@ SIGNATURES = {
     "mhc_strerror": (ctypes.c_char_p, [_I]),
     "mhc_set_trace": (_I, [_P, _I64]),
     "mhc_step_occupancy": (_I, [_I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "mhc_step_tile": (_I, [_I64, _I, _I, _U]),
     "mhc_version": (_I, []),
 }
 
@@ -118,6 +120,11 @@ def _need(t, dtype, name, device="cuda"):
 def split_flag(split: int) -> int:
     """Flag bits that force the number of CTAs splitting the width (1, 2, 4 or 8)."""
     return (split & 0xF) << SPLIT_SHIFT
+
+
+def tile_flag(tokens: int) -> int:
+    """Flag bits that force the tokens per tile (a multiple of 8, 8..128)."""
+    return ((tokens // 8) & 0x1F) << TILE_SHIFT
 
 
 def workspace_bytes(d: int, n: int = N_STREAMS) -> int:
@@ -342,6 +349,14 @@ def step_occupancy(d: int, flags: int = 0, n: int = N_STREAMS):
     _check(lib.mhc_step_occupancy(n, d, flags, ctypes.byref(sp), ctypes.byref(cl)),
            "mhc_step_occupancy")
     return sp.value, cl.value
+
+
+def step_tile(N: int, d: int, flags: int = 0, n: int = N_STREAMS) -> int:
+    """Tokens per tile the fused step uses for N tokens on the current device."""
+    rc = int(lib.mhc_step_tile(N, n, d, flags))
+    if rc < 0:
+        raise MhcError(rc, "mhc_step_tile")
+    return rc
 
 
 def set_trace(buffer=None):

@@ -76,6 +76,9 @@ def test_fused_validation(M):
     assert _fused(M, d=5000) == M.MHC_ERR_SHAPE          # not a multiple of the tile width (16*8)
     assert _fused(M, d=8192) == M.MHC_ERR_SHAPE          # slice too wide for TMEM at split 8
     assert _fused(M, flags=3 << 8) == M.MHC_ERR_SHAPE    # split 3 is not offered
+    assert _fused(M, flags=17 << 16) == M.MHC_ERR_SHAPE   # tile of 136 tokens: over 128
+    assert _fused(M, N=0, flags=M.tile_flag(96)) == M.MHC_OK
+    assert M.tile_flag(96) == 12 << 16
     assert _fused(M, flags=1 << 8) == M.MHC_ERR_SHAPE    # 5120 columns do not fit one CTA
     p = [_addr(i) for i in range(15)]
     p[0] = ctypes.c_void_p(A + 8)

@@ -180,3 +180,39 @@ def test_workload_sampled(M, synth, name):
     ref = oracle_step(sub)
     got = {k: v[idx.to(DEV)] for k, v in out.items()}
     check_step(got, ref)
+
+
+@pytest.mark.parametrize("N,d,tile", [
+    (300, 512, 8),           # 8-token tiles: 38 tiles, ragged last one
+    (1000, 5120, 40),        # rows 40..127 of every tile idle
+    (700, 2048, 96),
+    (330, 1024, 120),
+    (129, 256, 128),
+])
+def test_fused_tile_heights(M, synth, N, d, tile):
+    """Tiles shorter than the 128 TMEM lanes: rows at and past the tile height compute on stale
+    shared memory and are never stored; every token still matches the oracle."""
+    inp = synth.make_inputs(N, 4, d, seed=4000 + N + tile, device=DEV, scale_uniform=True,
+                            x_stream_std=True)
+    flags = M.tile_flag(tile)
+    assert M.step_tile(N, d, flags) == tile
+    out = _run(M, inp, flags=flags)
+    assert M.get_status() == M.MHC_OK
+    check_step(out, oracle_step(inp))
+
+
+def test_automatic_tile_choice(M):
+    """The automatic height minimises the busiest group's rounds x (height + fixed tile cost):
+    128 for the B=4, T=8192 batch (every smaller height costs more rounds than it saves), and a
+    shorter tile when that removes a round."""
+    split, groups = M.step_occupancy(5120)
+
+    def cost(N, t):
+        return -(-(-(-N // t)) // groups) * (t + 96)
+    for N in (256, 4096, 32768, 131072, 1000):
+        tile = M.step_tile(N, 5120)
+        assert tile % 8 == 0 and 8 <= tile <= 128
+        assert cost(N, tile) == min(cost(N, t) for t in range(8, 129, 8)), N
+    if groups == 19:
+        assert M.step_tile(32768, 5120) == 128
+        assert M.step_tile(4096, 5120) == 112
