@@ -49,13 +49,14 @@ extern "C" {
 /* Test hook: one thread per CTA waits on a barrier that nothing completes, with a ~2 ms limit;
  * the wait gives up, records MHC_ERR_TIMEOUT for mhc_get_status, and the call completes.      */
 #define MHC_DEBUG_NEVER_ARRIVE   0x2u
-/* Bits 8..11: number of CTAs (1, 2, 4 or 8) that split the width d of each token tile between
- * them (a group of co-resident CTAs). 0 = automatic (the fewest that fit on chip).            */
+/* Bits 8..11: log2 + 1 of the number of CTAs (1, 2, 4, 8, 16 or 32) that split the width d of
+ * each token tile between them (a group of co-resident CTAs); values above 6 are MHC_ERR_SHAPE.
+ * 0 = automatic: with the tile height (below), the shape that minimises the busiest group's
+ * work: wider groups for few tokens, the fewest CTAs per tile for many.                       */
 #define MHC_SPLIT_SHIFT          8
 #define MHC_SPLIT_MASK           (0xFu << MHC_SPLIT_SHIFT)
 /* Bits 16..20: tokens per tile of the step kernel / 8 (1..16, i.e. 8..128 tokens; larger values
- * are MHC_ERR_SHAPE). 0 = automatic: the height that minimises the busiest group's share of the
- * tiles (plus a fixed cost per tile), so the last round of tiles keeps every group busy.       */
+ * are MHC_ERR_SHAPE; the height must be a multiple of the split). 0 = automatic (above).      */
 #define MHC_TILE_SHIFT           16
 #define MHC_TILE_MASK            (0x1Fu << MHC_TILE_SHIFT)
 
@@ -98,8 +99,9 @@ size_t mhc_workspace_bytes(int n, int d);
  *   X_out     bf16 [N, n, d]      may equal X (in place); no other overlap
  *   y_out     bf16 [N, d]
  *   pre_out, post_out fp32 [N, n]; comb_out fp32 [N, n, n]; mixes_out fp32 [N, (2+n)n] or NULL
- *   d: for the chosen split, d/split must be a multiple of 2B (B = mhc_packed_block_columns())
- *      between 4B and 640 (d = 5120 uses split 8).
+ *   d: for some split of 1, 2, 4, 8, 16 or 32 CTAs per tile, d/split is a multiple of 2B
+ *      (B = mhc_packed_block_columns()) between 4B and 640; d = 5120 runs with 8 or 16 CTAs
+ *      per tile, d <= 20480 at most.
  *   workspace: >= mhc_workspace_bytes(n, d) device bytes; W_mix is packed into its start each
  *      call and the rest is the step scratch. Calls that share a workspace or scratch buffer
  *      must not overlap in time on the GPU (put them on one stream).
@@ -236,12 +238,10 @@ int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* str
  * MHC_ERR_TIMEOUT if a bounded device-side wait gave up since the last call, or MHC_ERR_CUDA
  * if the synchronisation itself failed.                                                       */
 int mhc_get_status(void* stream);
-/* Launch shape of the fused step on the current device: the width split it uses for (n, d,
- * flags) and how many groups of `split` CTAs the device holds at once. Diagnostic; needs a GPU. */
-int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* groups);
-/* Tokens per tile the fused step uses for N tokens of width d with `flags` on the current device
- * (see MHC_TILE_SHIFT), or a negative code. Diagnostic; needs a GPU.                          */
-int mhc_step_tile(int64_t N, int n, int d, unsigned flags);
+/* Launch shape of the fused step (and of mhc_mixes) for N tokens of width d with `flags` on
+ * the current device: CTAs that share a tile, tokens per tile, and groups launched (each group
+ * is `split` CTAs, one per SM). Diagnostic; needs a GPU.                                      */
+int mhc_step_config(int64_t N, int n, int d, unsigned flags, int* split, int* tile, int* groups);
 /* Phase tracing of the fused step (off by default). With a device buffer set, every later
  * launch whose grid fits records, per CTA, 8 uint64 values from the GPU's nanosecond timer:
  * the start time, then nanoseconds since the start at: loads issued, main loop done, partials

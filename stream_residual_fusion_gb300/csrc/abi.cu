@@ -52,10 +52,14 @@ namespace {
 // Checks shared by the fused step and the mixes call. Returns MHC_OK and the split, or a code.
 int check_step_shape(int64_t N, int n, int d, int iters, unsigned flags, int* split) {
   if (n != 4 || N < 0 || N > kMaxTokens || iters < 1 || d <= 0) return MHC_ERR_SHAPE;
-  const int forced = static_cast<int>((flags & MHC_SPLIT_MASK) >> MHC_SPLIT_SHIFT);
-  *split = choose_split(d, forced);
-  if (tile_flag(flags) < 0) return MHC_ERR_SHAPE;
-  return *split == 0 ? MHC_ERR_SHAPE : MHC_OK;
+  const int fs = split_flag_value(flags), ft = tile_flag(flags);
+  if (fs < 0 || ft < 0) return MHC_ERR_SHAPE;
+  *split = choose_split(d, fs);
+  if (*split == 0) return MHC_ERR_SHAPE;
+  // some split that fits d must also divide a forced tile height
+  for (int s = 1; s <= kMaxSplit; s *= 2)
+    if ((fs == 0 || s == fs) && split_ok(d, s) && (ft == 0 || ft % s == 0)) return MHC_OK;
+  return MHC_ERR_SHAPE;
 }
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
@@ -332,21 +336,18 @@ const char* mhc_strerror(int code) {
   }
 }
 
-int mhc_step_occupancy(int n, int d, unsigned flags, int* split, int* clusters) {
-  if (!split || !clusters) return MHC_ERR_NULL;
-  int sp = 0;
-  const int rc = check_step_shape(0, n, d, 1, flags, &sp);
-  if (rc != MHC_OK) return rc;
-  *split = sp;
-  return cuda_code(step_occupancy(sp, clusters));
-}
-
-int mhc_step_tile(int64_t N, int n, int d, unsigned flags) {
-  int sp = 0, groups = 0;
+int mhc_step_config(int64_t N, int n, int d, unsigned flags, int* split, int* tile, int* groups) {
+  if (!split || !tile || !groups) return MHC_ERR_NULL;
+  int sp = 0, ctas = 0;
   const int rc = check_step_shape(N, n, d, 1, flags, &sp);
   if (rc != MHC_OK) return rc;
-  if (step_occupancy(sp, &groups) != cudaSuccess || groups < 1) return MHC_ERR_CUDA;
-  return choose_tile(N, groups, tile_flag(flags));
+  if (step_resident_ctas(&ctas) != cudaSuccess) return MHC_ERR_CUDA;
+  const StepShape sh = choose_shape(N, d, ctas, split_flag_value(flags), tile_flag(flags));
+  if (sh.split == 0) return MHC_ERR_CUDA;
+  *split = sh.split;
+  *tile = sh.tt;
+  *groups = sh.groups;
+  return MHC_OK;
 }
 
 // ---------------------------------------------------------------------------------------------

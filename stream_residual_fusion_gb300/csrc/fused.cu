@@ -412,17 +412,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto rms_factor = [&](int it_) {
       const unsigned target = static_cast<unsigned>(((it_ >> 1) + 1) * split * NCONS);
       if (!gwait(&syready[it_ & 1], target, limit())) timed_out = true;
-      float v[8];
-#pragma unroll
-      for (int rk = 0; rk < 8; ++rk) {   // row tail (S_x h0, S_x h1, S_y h0, S_y h1) of every rank
-        if (rk < split) {
-          const float4 q4 = __ldcg(reinterpret_cast<const float4*>(gpart(it_ & 1, rk) + tl * PART_STRIDE + 24));
-          v[rk] = q4.z + q4.w;
-        } else {
-          v[rk] = 0.f;
-        }
+      float sy = 0.f;
+      for (int rk = 0; rk < split; ++rk) {   // row tail (S_x h0, S_x h1, S_y h0, S_y h1) of every rank
+        const float4 q4 = __ldcg(reinterpret_cast<const float4*>(gpart(it_ & 1, rk) + tl * PART_STRIDE + 24));
+        sy += q4.z + q4.w;
       }
-      const float sy = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
       const float r = __frsqrt_rn(__fdiv_rn(sy, static_cast<float>(d)) + P.norm_eps);
       return f2{r, r};
     };
@@ -790,31 +784,40 @@ cudaError_t resident_ctas(Kern kern, int* ctas) {
 
 }  // namespace
 
-int choose_split(int d, int forced) {
+bool split_ok(int d, int s) {
   // slices of whole accumulation groups, at least 128 columns (the previous tile's RMS factor
   // is taken after slot RLAG - 1), and a stash ring of S + RLAG slots that fits TMEM
-  auto ok = [d](int s) {
-    return d > 0 && d % (DC * PG * s) == 0 && d / s <= MAX_SLICE && d / s >= 4 * WDC;
-  };
-  if (forced != 0) return (forced == 1 || forced == 2 || forced == 4 || forced == 8) && ok(forced) ? forced : 0;
-  for (int s : {1, 2, 4, 8})
-    if (ok(s)) return s;
+  return d > 0 && s >= 1 && s <= kMaxSplit && d % (DC * PG * s) == 0 && d / s <= MAX_SLICE &&
+         d / s >= 4 * WDC;
+}
+
+int choose_split(int d, int forced) {
+  if (forced != 0) return split_ok(d, forced) ? forced : 0;
+  for (int s = 1; s <= kMaxSplit; s *= 2)
+    if (split_ok(d, s)) return s;
   return 0;
 }
 
-int choose_tile(int64_t N, int groups, int forced) {
-  if (forced != 0) return forced;
-  // the tile height that minimises the busiest group's work, ceil(tiles / groups) tiles of tt
-  // tokens each plus a fixed cost per tile; ties go to the taller tile
-  int best = TT;
+StepShape choose_shape(int64_t N, int d, int ctas, int forced_split, int forced_tile) {
+  // Every tile runs d / (DC * split) pipeline slots, each costing about (tt + kTileCostTokens)
+  // tokens' worth of time; a group handles ceil(tiles / groups) tiles. Minimise the busiest
+  // group's total; ties go to the smaller split and then the taller tile.
+  StepShape best{0, 0, 0};
   int64_t best_cost = INT64_MAX;
-  for (int tt = TT; tt >= 8; tt -= 8) {
-    const int64_t tiles = (N + tt - 1) / tt;
-    const int64_t rounds = (tiles + groups - 1) / groups;
-    const int64_t cost = rounds * (tt + kTileCostTokens);
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = tt;
+  const int64_t n = std::max<int64_t>(N, 1);
+  for (int s = 1; s <= kMaxSplit; s *= 2) {
+    if ((forced_split != 0 && s != forced_split) || !split_ok(d, s) || ctas < s) continue;
+    const int groups = ctas / s;
+    const int64_t slots = d / (DC * s);
+    for (int tt = TT; tt >= 8; tt -= 8) {
+      if ((forced_tile != 0 && tt != forced_tile) || tt % s != 0) continue;
+      const int64_t tiles = (n + tt - 1) / tt;
+      const int64_t rounds = (tiles + groups - 1) / groups;
+      const int64_t cost = rounds * slots * (tt + kTileCostTokens);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = StepShape{s, tt, static_cast<int>(std::min<int64_t>(tiles, groups))};
+      }
     }
   }
   return best;
@@ -837,10 +840,12 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   int ctas = 0;
   e = resident_ctas(kern, &ctas);
   if (e != cudaSuccess) return e;
-  if (ctas < a.split) return cudaErrorInvalidConfiguration;
-  const int tt = choose_tile(a.N, ctas / a.split, tile_flag(a.flags));
+  const StepShape shape = choose_shape(a.N, a.d, ctas, split_flag_value(a.flags), tile_flag(a.flags));
+  if (shape.split == 0) return cudaErrorInvalidConfiguration;
+  const int split = shape.split;
+  const int tt = shape.tt;
+  const int ngroups = std::max(1, shape.groups);
   const int tiles = static_cast<int>((a.N + tt - 1) / tt);
-  const int ngroups = std::max(1, std::min(tiles, ctas / a.split));
   CUtensorMap tx, tf, txo, ty;
   if (!map_streams(&tx, a.X, a.N, a.d, tt)) return cudaErrorInvalidValue;
   if (fused) {
@@ -867,19 +872,19 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   P.mixes_out = a.mixes_out;
   P.status = status_word();
   if (P.status == nullptr) return cudaErrorInvalidDevice;
-  P.trace = trace_buffer(static_cast<int64_t>(a.split) * tiles);
+  P.trace = trace_buffer(static_cast<int64_t>(split) * tiles);
   // scratch: [256 B of group counters per 8 groups ... ] then the partial sums
   uint8_t* scratch = static_cast<uint8_t*>(a.scratch);
   const size_t counter_bytes = (static_cast<size_t>(ngroups) * 32 + 255) / 256 * 256;
   P.counters = reinterpret_cast<unsigned*>(scratch);
   P.gpart = reinterpret_cast<float*>(scratch + counter_bytes);
-  if (counter_bytes + static_cast<size_t>(ngroups) * a.split * 2 * PART_BYTES > a.scratch_bytes)
+  if (counter_bytes + static_cast<size_t>(ngroups) * split * 2 * PART_BYTES > a.scratch_bytes)
     return cudaErrorInvalidValue;
   P.N = static_cast<int>(a.N);
   P.tt = tt;
   P.d = a.d;
-  P.split = a.split;
-  P.slice = a.d / a.split;
+  P.split = split;
+  P.slice = a.d / split;
   P.nsteps = P.slice / DC;
   P.iters = a.iters;
   P.hc_eps = a.hc_eps;
@@ -889,7 +894,7 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   e = cudaMemsetAsync(P.counters, 0, static_cast<size_t>(ngroups) * 32, stream);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ngroups * a.split, 1, 1);
+  cfg.gridDim = dim3(ngroups * split, 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
@@ -901,14 +906,11 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kern, tx, tf, txo, ty, P);
 }
 
-cudaError_t step_occupancy(int split, int* groups) {
+cudaError_t step_resident_ctas(int* ctas) {
   auto kern = step_kernel<true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  int ctas = 0;
-  e = resident_ctas(kern, &ctas);
-  if (e == cudaSuccess) *groups = ctas / split;
-  return e;
+  return resident_ctas(kern, ctas);
 }
 
 }  // namespace mhc

@@ -39,26 +39,41 @@ struct StepArgs {
   unsigned flags;
 };
 
-// Returns the split (1, 2, 4 or 8) the step kernel uses for width d, or 0 if d is not supported.
-// `forced` = 0 picks automatically.
+// Largest number of CTAs that share a tile.
+constexpr int kMaxSplit = 32;
+// Whether `split` CTAs can share a tile of width d.
+bool split_ok(int d, int split);
+// The smallest split that fits width d (or `forced` if it fits); 0 if none.
 int choose_split(int d, int forced);
-// Tokens per tile of the step kernel for N tokens on `groups` groups (a multiple of 8, <= 128);
-// `forced` != 0 is returned as is.
-int choose_tile(int64_t N, int groups, int forced);
-// The fixed cost of a tile, in tokens of streaming work, that choose_tile charges per tile.
-// Measured on GB300 at d = 5120: a tile of tt tokens takes about (tt + 96) tokens' worth of
-// time (every tile runs its 20 pipeline slots, each paying load latency), e.g. 685 us for 256
-// tiles of 128 tokens against 955 us for 512 tiles of 64.
+// Launch shape of the step kernel: CTAs per tile, tokens per tile (a multiple of 8 and of the
+// split, <= 128) and groups launched. `forced_*` != 0 pins a value; split 0 if nothing fits.
+struct StepShape {
+  int split;
+  int tt;
+  int groups;
+};
+StepShape choose_shape(int64_t N, int d, int ctas, int forced_split, int forced_tile);
+// Cost of one pipeline slot of the step kernel in tokens of streaming work: a slot of a tile of
+// tt tokens takes about (tt + kTileCostTokens) units (every slot pays load latency). Measured on
+// GB300 at d = 5120, 20 slots per tile: 685 us for 256 tiles of 128 tokens, 955 us for 512
+// tiles of 64.
 constexpr int kTileCostTokens = 96;
 // Tile height forced by the flags (MHC_TILE_SHIFT bits), 0 if automatic; -1 if invalid.
 inline int tile_flag(unsigned flags) {
   const int v = static_cast<int>((flags >> 16) & 0x1Fu);
   return v == 0 ? 0 : (v <= 16 ? 8 * v : -1);
 }
+// Split forced by the flags (MHC_SPLIT_SHIFT bits hold log2(split) + 1), 0 if automatic; -1 if
+// invalid.
+inline int split_flag_value(unsigned flags) {
+  const int v = static_cast<int>((flags >> 8) & 0xFu);
+  return v == 0 ? 0 : (v <= 6 ? 1 << (v - 1) : -1);
+}
 constexpr int kMaxTokens = 65535 * 128;
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream);
-cudaError_t step_occupancy(int split, int* groups);
+// CTAs of the step kernel the current device holds at once (one per SM).
+cudaError_t step_resident_ctas(int* ctas);
 // Scratch the step kernel needs on the current device (0 if the device cannot be queried).
 size_t step_scratch_bytes();
 cudaError_t launch_pack(const float* W, void* packed, int d, cudaStream_t stream);

@@ -71,8 +71,8 @@ SIGNATURES = {
     "mhc_get_status": (_I, [_P]),
     "mhc_strerror": (ctypes.c_char_p, [_I]),
     "mhc_set_trace": (_I, [_P, _I64]),
-    "mhc_step_occupancy": (_I, [_I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
-    "mhc_step_tile": (_I, [_I64, _I, _I, _U]),
+    "mhc_step_config": (_I, [_I64, _I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                             ctypes.POINTER(_I)]),
     "mhc_version": (_I, []),
 }
 
@@ -118,8 +118,13 @@ def _need(t, dtype, name, device="cuda"):
 
 
 def split_flag(split: int) -> int:
-    """Flag bits that force the number of CTAs splitting the width (1, 2, 4 or 8)."""
-    return (split & 0xF) << SPLIT_SHIFT
+    """Flag bits that force the number of CTAs splitting the width (1, 2, 4, 8, 16 or 32; 0 =
+    automatic)."""
+    if split == 0:
+        return 0
+    if split < 1 or split & (split - 1):
+        raise ValueError("split must be a power of two")
+    return (split.bit_length() & 0xF) << SPLIT_SHIFT
 
 
 def tile_flag(tokens: int) -> int:
@@ -343,20 +348,12 @@ def hc_pre(Xp, pre, out=None, stream=None):
     return y
 
 
-def step_occupancy(d: int, flags: int = 0, n: int = N_STREAMS):
-    """(split, clusters resident at once) of the fused step on the current device."""
-    sp, cl = _I(0), _I(0)
-    _check(lib.mhc_step_occupancy(n, d, flags, ctypes.byref(sp), ctypes.byref(cl)),
-           "mhc_step_occupancy")
-    return sp.value, cl.value
-
-
-def step_tile(N: int, d: int, flags: int = 0, n: int = N_STREAMS) -> int:
-    """Tokens per tile the fused step uses for N tokens on the current device."""
-    rc = int(lib.mhc_step_tile(N, n, d, flags))
-    if rc < 0:
-        raise MhcError(rc, "mhc_step_tile")
-    return rc
+def step_config(N: int, d: int, flags: int = 0, n: int = N_STREAMS):
+    """(split, tokens per tile, groups) of the fused step for N tokens on the current device."""
+    sp, tt, gr = _I(0), _I(0), _I(0)
+    _check(lib.mhc_step_config(N, n, d, flags, ctypes.byref(sp), ctypes.byref(tt), ctypes.byref(gr)),
+           "mhc_step_config")
+    return sp.value, tt.value, gr.value
 
 
 def set_trace(buffer=None):

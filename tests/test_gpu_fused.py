@@ -44,6 +44,9 @@ CASES = [
     (300, 5120, 0),
     (130, 640, 1),           # widest slice the TMEM stash ring holds (640 columns)
     (260, 128, 1),           # narrowest slice (4 stages)
+    (300, 5120, 16),         # 16 CTAs per tile, 320 columns each
+    (200, 8192, 16),
+    (160, 4096, 32),         # 32 CTAs per tile, the narrowest slices
 ]
 
 
@@ -195,24 +198,27 @@ def test_fused_tile_heights(M, synth, N, d, tile):
     inp = synth.make_inputs(N, 4, d, seed=4000 + N + tile, device=DEV, scale_uniform=True,
                             x_stream_std=True)
     flags = M.tile_flag(tile)
-    assert M.step_tile(N, d, flags) == tile
+    assert M.step_config(N, d, flags)[1] == tile
     out = _run(M, inp, flags=flags)
     assert M.get_status() == M.MHC_OK
     check_step(out, oracle_step(inp))
 
 
-def test_automatic_tile_choice(M):
-    """The automatic height minimises the busiest group's rounds x (height + fixed tile cost):
-    128 for the B=4, T=8192 batch (every smaller height costs more rounds than it saves), and a
-    shorter tile when that removes a round."""
-    split, groups = M.step_occupancy(5120)
+def test_automatic_shape_choice(M):
+    """The automatic launch shape minimises the busiest group's rounds x slots x (height + fixed
+    slot cost) over the splits that fit and the heights that are multiples of the split: the
+    fewest CTAs per tile and 128-token tiles for the B=4, T=8192 batch, wider groups for decode."""
+    split, _, groups = M.step_config(32768, 5120)
+    ctas = split * groups
 
-    def cost(N, t):
-        return -(-(-(-N // t)) // groups) * (t + 96)
+    def cost(N, s, t):
+        return -(-(-(-N // t)) // (ctas // s)) * (5120 // (32 * s)) * (t + 96)
     for N in (256, 4096, 32768, 131072, 1000):
-        tile = M.step_tile(N, 5120)
-        assert tile % 8 == 0 and 8 <= tile <= 128
-        assert cost(N, tile) == min(cost(N, t) for t in range(8, 129, 8)), N
-    if groups == 19:
-        assert M.step_tile(32768, 5120) == 128
-        assert M.step_tile(4096, 5120) == 112
+        split, tile, groups = M.step_config(N, 5120)
+        assert tile % 8 == 0 and 8 <= tile <= 128 and tile % split == 0
+        options = [cost(N, s, t) for s in (8, 16) for t in range(128, 7, -8) if t % s == 0]
+        assert cost(N, split, tile) == min(options), N
+    if ctas == 152:
+        assert M.step_config(32768, 5120)[:2] == (8, 128)
+        assert M.step_config(4096, 5120)[:2] == (8, 112)
+        assert M.step_config(256, 5120)[:2] == (16, 32)
