@@ -99,9 +99,9 @@ size_t mhc_workspace_bytes(int n, int d);
  *   X_out     bf16 [N, n, d]      may equal X (in place); no other overlap
  *   y_out     bf16 [N, d]
  *   pre_out, post_out fp32 [N, n]; comb_out fp32 [N, n, n]; mixes_out fp32 [N, (2+n)n] or NULL
- *   d: for some split of 1, 2, 4, 8, 16 or 32 CTAs per tile, d/split is a multiple of 2B
- *      (B = mhc_packed_block_columns()) between 4B and 640; d = 5120 runs with 8 or 16 CTAs
- *      per tile, d <= 20480 at most.
+ *   d: for some split of 1, 2, 4, 8, 16 or 32 CTAs per tile, d/split is a multiple of B
+ *      (B = mhc_packed_block_columns()) between 4B and 640; d = 5120 runs with 8, 16 or 32
+ *      CTAs per tile, d <= 20480 at most.
  *   workspace: >= mhc_workspace_bytes(n, d) device bytes; W_mix is packed into its start each
  *      call and the rest is the step scratch. Calls that share a workspace or scratch buffer
  *      must not overlap in time on the GPU (put them on one stream).

@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int col0 = static_cast<int>(g) * DC;          // first column of this CTA's slice
   const int cstride = DC * split;                     // stride between its slots' columns
   const int S = P.nsteps;                             // slots per tile
-  const int G = S / PG;                               // accumulation groups per tile
+  const int G = (S + PG - 1) / PG;                    // accumulation groups per tile (the last
+                                                      // may hold fewer slots)
   const int R = S + RLAG;                             // y_hat stash ring slots
   const int d = P.d;
   bool timed_out = false;
@@ -297,14 +298,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       };
       for (int u = 0; u < NW && u < nblocks; ++u) load_block(u);
       int gs = 0;
-      for (int tile = c0; tile < ntiles; tile += nclust) {
+      for (int tile = c0, it = 0; tile < ntiles; tile += nclust, ++it) {
         for (int s = 0; s < S; ++s, ++gs) {
           const int b = gs % NSTAGE;
           if (!mbar_wait(FUSED ? &xready[b] : &full[b], (gs / NSTAGE) & 1, limit())) timed_out = true;
           tc_fence_after();
-          // accumulation groups of PG slots alternate between the two accumulators; slices hold
-          // whole groups, so gs % PG == s % PG
-          const int gg = gs / PG;
+          // accumulation groups of PG slots (numbered across tiles) alternate between the two
+          // accumulators
+          const int gg = it * G + s / PG;
           const uint32_t acc = tmem + static_cast<uint32_t>((gg & 1) * ACC_COLS);
 #pragma unroll
           for (int j = 0; j < HALVES; ++j) {
@@ -412,10 +413,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto rms_factor = [&](int it_) {
       const unsigned target = static_cast<unsigned>(((it_ >> 1) + 1) * split * NCONS);
       if (!gwait(&syready[it_ & 1], target, limit())) timed_out = true;
+      // S_y of both halves of every rank's row, eight ranks' loads in flight at a time
       float sy = 0.f;
-      for (int rk = 0; rk < split; ++rk) {   // row tail (S_x h0, S_x h1, S_y h0, S_y h1) of every rank
-        const float4 q4 = __ldcg(reinterpret_cast<const float4*>(gpart(it_ & 1, rk) + tl * PART_STRIDE + 24));
-        sy += q4.z + q4.w;
+      for (int rk0 = 0; rk0 < split; rk0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          v[u] = 0.f;
+          if (rk0 + u < split) {
+            const float2 q2 = __ldcg(reinterpret_cast<const float2*>(gpart(it_ & 1, rk0 + u) + tl * PART_STRIDE + 26));
+            v[u] = q2.x + q2.y;
+          }
+        }
+        sy += ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
       }
       const float r = __frsqrt_rn(__fdiv_rn(sy, static_cast<float>(d)) + P.norm_eps);
       return f2{r, r};
@@ -564,7 +574,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // Fold group q in the last slot of group q+1 (global numbering, across tiles): the MMA
         // that reuses q's accumulator (group q+2) starts only after this warp's xready of a
         // later slot.
-        if (gs % PG == PG - 1 && gs >= 2 * PG - 1) fold(folded++);
+        if ((s % PG == PG - 1 || s == S - 1) && it * G + s / PG >= 1) fold(folded++);
         // the previous tile's RMS factor, needed from slot RLAG on: fetched after slot RLAG-1's
         // work is published, so the wait overlaps that slot's MMAs and stores
         if (FUSED && s == RLAG - 1 && it > 0) r_new = rms_factor(it - 1);
@@ -628,64 +638,145 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ------------------------------------------------------------------ finisher
-    // Tokens [g*per, (g+1)*per) of each tile: scale, split, Sinkhorn; four lanes per token,
-    // lane j owning comb row j, 8 tokens per pass.
+    // Tokens [g*per, (g+1)*per) of each tile: scale, split, Sinkhorn. Two layouts, by tokens per
+    // CTA (uniform over the launch):
+    //   * per >= 8: the finisher runs beside the main loop, so it is kept lean. 16 tokens per
+    //     pass; lane 4q + j serves tokens q and q + 8 and owns comb row j; it sums, rank by rank,
+    //     only the 16 partial sums its row needs; the token's four lanes run Sinkhorn together
+    //     (split_sinkhorn_row, shuffles for the column sums).
+    //   * per < 8: few tokens per CTA, the finisher is on the critical path. TP tokens per pass
+    //     (up to 8), L = 32 / TP lanes per token: lane r of a token adds the rows of ranks r,
+    //     r + L, ... (two ranks' loads in flight at a time), a shuffle butterfly combines the L
+    //     sums (the same total in every lane), and every lane runs the whole Sinkhorn
+    //     (split_sinkhorn_all, no shuffle latency); lanes r < 4 write row r.
     const int q = lane >> 2;
     const int j = lane & 3;
     const int per = tt / split;
+    int TP = 8;
+    while (TP > 1 && TP > per) TP >>= 1;
+    const int L = 32 / TP;
+    const int lq = lane / L;
+    const int lr = lane % L;
     int it = 0;
     for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
       const int pb = it & 1;
       if (!gwait(&pready[pb], static_cast<unsigned>(((it >> 1) + 1) * split * NCONS), limit()))
         timed_out = true;
       const int t0 = tile * tt;
-      // 16 tokens per pass (two per lane group); after the last pass's reads the peers may
-      // reuse their partials buffers
-      for (int base_t = 0; base_t < per; base_t += 16) {
-        float4 s0[2], s1[2], s2[2], s6[2];
+      if (per >= 8) {
+        // 16 tokens per pass (two per lane group); after the last pass's reads the peers may
+        // reuse their partials buffers
+        for (int base_t = 0; base_t < per; base_t += 16) {
+          float4 s0[2], s1[2], s2[2], s6[2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          s0[u] = s1[u] = s2[u] = s6[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          const int tl2 = static_cast<int>(g) * per + min(base_t + 8 * u + q, per - 1);
-          for (int rk = 0; rk < split; ++rk) {
-            const float4* row = reinterpret_cast<const float4*>(gpart(pb, rk) + tl2 * PART_STRIDE);
-            const float4 v0 = __ldcg(row);
-            const float4 v1 = __ldcg(row + 1);
-            const float4 v2 = __ldcg(row + 2 + j);
-            const float4 v6 = __ldcg(row + 6);
-            s0[u].x += v0.x; s0[u].y += v0.y; s0[u].z += v0.z; s0[u].w += v0.w;
-            s1[u].x += v1.x; s1[u].y += v1.y; s1[u].z += v1.z; s1[u].w += v1.w;
-            s2[u].x += v2.x; s2[u].y += v2.y; s2[u].z += v2.z; s2[u].w += v2.w;
-            s6[u].x += v6.x + v6.y;
+          for (int u = 0; u < 2; ++u) {
+            s0[u] = s1[u] = s2[u] = s6[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int tl2 = static_cast<int>(g) * per + min(base_t + 8 * u + q, per - 1);
+            for (int rk = 0; rk < split; ++rk) {
+              const float4* row = reinterpret_cast<const float4*>(gpart(pb, rk) + tl2 * PART_STRIDE);
+              const float4 v0 = __ldcg(row);
+              const float4 v1 = __ldcg(row + 1);
+              const float4 v2 = __ldcg(row + 2 + j);
+              const float4 v6 = __ldcg(row + 6);
+              s0[u].x += v0.x; s0[u].y += v0.y; s0[u].z += v0.z; s0[u].w += v0.w;
+              s1[u].x += v1.x; s1[u].y += v1.y; s1[u].z += v1.z; s1[u].w += v1.w;
+              s2[u].x += v2.x; s2[u].y += v2.y; s2[u].z += v2.z; s2[u].w += v2.w;
+              s6[u].x += v6.x + v6.y;
+            }
+          }
+          if (base_t + 16 >= per) {
+            // every read of buffer pb is done: the group may reuse it
+            __syncwarp();
+            if (lane == 0) gcount_release(&pfree[pb]);
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int tk = base_t + 8 * u + q;
+            const bool in_range = tk < per;
+            const int token2 = t0 + static_cast<int>(g) * per + tk;
+            const float rs = __frsqrt_rn(__fdiv_rn(s6[u].x, static_cast<float>(4 * d)) + P.norm_eps);
+            const float m0[4] = {s0[u].x * rs, s0[u].y * rs, s0[u].z * rs, s0[u].w * rs};
+            const float m1[4] = {s1[u].x * rs, s1[u].y * rs, s1[u].z * rs, s1[u].w * rs};
+            const float mrow[4] = {s2[u].x * rs, s2[u].y * rs, s2[u].z * rs, s2[u].w * rs};
+            float pj, uj, crow[4];
+            split_sinkhorn_row(mrow, m0[j], m1[j], j, __ldg(P.scale), __ldg(P.scale + 1),
+                               __ldg(P.scale + 2), P.base, P.iters, P.hc_eps, pj, uj, crow);
+            if (in_range && token2 < P.N) {
+              P.pre_out[static_cast<size_t>(token2) * 4 + j] = pj;
+              P.post_out[static_cast<size_t>(token2) * 4 + j] = uj;
+              reinterpret_cast<float4*>(P.comb_out + static_cast<size_t>(token2) * 16)[j] =
+                  make_float4(crow[0], crow[1], crow[2], crow[3]);
+              if (P.mixes_out != nullptr) {
+                float4* mo = reinterpret_cast<float4*>(P.mixes_out + static_cast<size_t>(token2) * 24);
+                mo[2 + j] = make_float4(mrow[0], mrow[1], mrow[2], mrow[3]);
+                if (j == 0) mo[0] = make_float4(m0[0], m0[1], m0[2], m0[3]);
+                if (j == 1) mo[1] = make_float4(m1[0], m1[1], m1[2], m1[3]);
+              }
+            }
           }
         }
-        if (base_t + 16 >= per) {
-          // every read of buffer pb is done: the group may reuse it
-          __syncwarp();
-          if (lane == 0) gcount_release(&pfree[pb]);
-        }
+      } else {
+        for (int base_t = 0; base_t < per; base_t += TP) {
+          const int tt_ = base_t + lq;
+          const bool in_range = tt_ < per;
+          const int tl2 = static_cast<int>(g) * per + min(tt_, per - 1);
+          float acc[26];   // 24 mix sums, then S_x of both halves
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int tt = base_t + 8 * u + q;
-          const bool in_range = tt < per;
-          const int token2 = t0 + static_cast<int>(g) * per + tt;
-          const float rs = __frsqrt_rn(__fdiv_rn(s6[u].x, static_cast<float>(4 * d)) + P.norm_eps);
-          const float m0[4] = {s0[u].x * rs, s0[u].y * rs, s0[u].z * rs, s0[u].w * rs};
-          const float m1[4] = {s1[u].x * rs, s1[u].y * rs, s1[u].z * rs, s1[u].w * rs};
-          const float mrow[4] = {s2[u].x * rs, s2[u].y * rs, s2[u].z * rs, s2[u].w * rs};
-          float pj, uj, crow[4];
-          split_sinkhorn_row(mrow, m0[j], m1[j], j, __ldg(P.scale), __ldg(P.scale + 1),
-                             __ldg(P.scale + 2), P.base, P.iters, P.hc_eps, pj, uj, crow);
-          if (in_range && token2 < P.N) {
-            P.pre_out[static_cast<size_t>(token2) * 4 + j] = pj;
-            P.post_out[static_cast<size_t>(token2) * 4 + j] = uj;
-            reinterpret_cast<float4*>(P.comb_out + static_cast<size_t>(token2) * 16)[j] =
+          for (int e = 0; e < 26; ++e) acc[e] = 0.f;
+          for (int rk = lr; rk < split; rk += 2 * L) {
+            const bool two = rk + L < split;
+            const float4* r0 = reinterpret_cast<const float4*>(gpart(pb, rk) + tl2 * PART_STRIDE);
+            const float4* r1 = reinterpret_cast<const float4*>(gpart(pb, two ? rk + L : rk) + tl2 * PART_STRIDE);
+            float4 v0[7], v1[7];
+#pragma unroll
+            for (int e = 0; e < 7; ++e) {
+              v0[e] = __ldcg(r0 + e);
+              v1[e] = two ? __ldcg(r1 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int e = 0; e < 7; ++e) {
+              const float a4[4] = {v0[e].x + v1[e].x, v0[e].y + v1[e].y, v0[e].z + v1[e].z, v0[e].w + v1[e].w};
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                if (4 * e + c < 26) acc[4 * e + c] += a4[c];
+            }
+          }
+          for (int off = 1; off < L; off <<= 1)
+#pragma unroll
+            for (int e = 0; e < 26; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+          if (base_t + TP >= per) {
+            // every read of buffer pb is done: the group may reuse it
+            __syncwarp();
+            if (lane == 0) gcount_release(&pfree[pb]);
+          }
+          const int token2 = t0 + static_cast<int>(g) * per + tt_;
+          const float rs = __frsqrt_rn(__fdiv_rn(acc[24] + acc[25], static_cast<float>(4 * d)) + P.norm_eps);
+          float m[24];
+#pragma unroll
+          for (int e = 0; e < 24; ++e) m[e] = acc[e] * rs;
+          float pv[4], uv[4], cv[16];
+          split_sinkhorn_all(m, __ldg(P.scale), __ldg(P.scale + 1), __ldg(P.scale + 2), P.base,
+                             P.iters, P.hc_eps, pv, uv, cv);
+          // lane r < 4 writes row r
+          const int jr = lr & 3;
+          const float pj = jr == 0 ? pv[0] : jr == 1 ? pv[1] : jr == 2 ? pv[2] : pv[3];
+          const float uj = jr == 0 ? uv[0] : jr == 1 ? uv[1] : jr == 2 ? uv[2] : uv[3];
+          float crow[4], mrow[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            crow[k] = jr == 0 ? cv[k] : jr == 1 ? cv[4 + k] : jr == 2 ? cv[8 + k] : cv[12 + k];
+            mrow[k] = jr == 0 ? m[8 + k] : jr == 1 ? m[12 + k] : jr == 2 ? m[16 + k] : m[20 + k];
+          }
+          if (in_range && lr < 4 && token2 < P.N) {
+            P.pre_out[static_cast<size_t>(token2) * 4 + jr] = pj;
+            P.post_out[static_cast<size_t>(token2) * 4 + jr] = uj;
+            reinterpret_cast<float4*>(P.comb_out + static_cast<size_t>(token2) * 16)[jr] =
                 make_float4(crow[0], crow[1], crow[2], crow[3]);
             if (P.mixes_out != nullptr) {
               float4* mo = reinterpret_cast<float4*>(P.mixes_out + static_cast<size_t>(token2) * 24);
-              mo[2 + j] = make_float4(mrow[0], mrow[1], mrow[2], mrow[3]);
-              if (j == 0) mo[0] = make_float4(m0[0], m0[1], m0[2], m0[3]);
-              if (j == 1) mo[1] = make_float4(m1[0], m1[1], m1[2], m1[3]);
+              mo[2 + jr] = make_float4(mrow[0], mrow[1], mrow[2], mrow[3]);
+              if (jr == 0) mo[0] = make_float4(m[0], m[1], m[2], m[3]);
+              if (jr == 1) mo[1] = make_float4(m[4], m[5], m[6], m[7]);
             }
           }
         }
@@ -785,9 +876,9 @@ cudaError_t resident_ctas(Kern kern, int* ctas) {
 }  // namespace
 
 bool split_ok(int d, int s) {
-  // slices of whole accumulation groups, at least 128 columns (the previous tile's RMS factor
+  // slices of whole slots, at least 128 columns (the previous tile's RMS factor
   // is taken after slot RLAG - 1), and a stash ring of S + RLAG slots that fits TMEM
-  return d > 0 && s >= 1 && s <= kMaxSplit && d % (DC * PG * s) == 0 && d / s <= MAX_SLICE &&
+  return d > 0 && s >= 1 && s <= kMaxSplit && d % (DC * s) == 0 && d / s <= MAX_SLICE &&
          d / s >= 4 * WDC;
 }
 

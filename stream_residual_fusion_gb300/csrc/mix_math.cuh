@@ -6,9 +6,12 @@
 //   L_jk = s_2 m_{8+4j+k} + b_{8+4j+k}
 //   C    = softmax over k (max subtracted) + eps; columns / (sum + eps);
 //          then (iters-1) x [rows / (sum + eps), columns / (sum + eps)].
-// split_sinkhorn: one thread owns one token. split_sinkhorn_row: four lanes own one token, lane j
-// holding row j of comb; column sums go through warp shuffles. Divisions by a row or column sum
-// are a reciprocal followed by a multiply (4 reciprocals instead of 16 divisions per step).
+// split_sinkhorn (standalone kernel): one thread owns one token. The fused kernel uses
+// split_sinkhorn_row (four lanes own one token, lane j holding row j of comb; column sums go
+// through warp shuffles) or split_sinkhorn_all (every lane of the token holds the whole matrix:
+// more arithmetic, no shuffle latency; for launches with few tokens per CTA). Divisions by a row
+// or column sum are a reciprocal followed by a multiply (4 reciprocals instead of 16 divisions
+// per step).
 #pragma once
 
 namespace mhc {
@@ -105,6 +108,53 @@ __device__ __forceinline__ void split_sinkhorn_row(const float (&mrow)[4], float
     const float r = rcp_approx(((c[0] + c[1]) + (c[2] + c[3])) + eps);
 #pragma unroll
     for (int k = 0; k < 4; ++k) c[k] *= r;
+    col_step();
+  }
+}
+
+// The same arithmetic as split_sinkhorn_row with one lane holding the whole 4 x 4 matrix (no
+// shuffles: each column sum is ((c0 + c1) + (c2 + c3)) over the rows, the value the row
+// version's butterfly leaves in every lane), so the two give bitwise the same result. Lanes that
+// run it on the same token hold the same result. Inputs: the 24 mix numbers m. Outputs: p, u,
+// comb.
+__device__ __forceinline__ void split_sinkhorn_all(const float (&m)[24], float s0, float s1,
+                                                   float s2, const float* __restrict__ base,
+                                                   int iters, float eps, float (&p)[4],
+                                                   float (&u)[4], float (&c)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    p[j] = sigmoid_f(fmaf(m[j], s0, __ldg(base + j))) + eps;
+    u[j] = 2.0f * sigmoid_f(fmaf(m[4 + j], s1, __ldg(base + 4 + j)));
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float* row = c + 4 * j;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) row[k] = fmaf(m[8 + 4 * j + k], s2, __ldg(base + 8 + 4 * j + k));
+    const float mx = fmaxf(fmaxf(row[0], row[1]), fmaxf(row[2], row[3]));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) row[k] = expf(row[k] - mx);
+    const float r = rcp_approx((row[0] + row[1]) + (row[2] + row[3]));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) row[k] = fmaf(row[k], r, eps);
+  }
+  auto col_step = [&]() {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float r = rcp_approx(((c[k] + c[4 + k]) + (c[8 + k] + c[12 + k])) + eps);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[4 * j + k] *= r;
+    }
+  };
+  col_step();
+  for (int it = 1; it < iters; ++it) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float* row = c + 4 * j;
+      const float r = rcp_approx(((row[0] + row[1]) + (row[2] + row[3])) + eps);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) row[k] *= r;
+    }
     col_step();
   }
 }

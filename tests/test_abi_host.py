@@ -79,7 +79,8 @@ def test_fused_validation(M):
     assert _fused(M, flags=7 << 8) == M.MHC_ERR_SHAPE    # split 64 is not offered
     assert _fused(M, flags=M.split_flag(4)) == M.MHC_ERR_SHAPE   # 1280 columns per CTA: too wide
     assert _fused(M, N=0, flags=M.split_flag(16)) == M.MHC_OK    # 320 columns per CTA
-    assert _fused(M, flags=M.split_flag(32)) == M.MHC_ERR_SHAPE  # 160: not whole accumulation groups
+    assert _fused(M, N=0, flags=M.split_flag(32)) == M.MHC_OK    # 160 columns: 5 slots
+    assert _fused(M, flags=M.split_flag(32) | M.tile_flag(16)) == M.MHC_ERR_SHAPE  # 16 % 32 != 0
     assert _fused(M, flags=M.split_flag(16) | M.tile_flag(8)) == M.MHC_ERR_SHAPE  # 8 % 16 != 0
     assert _fused(M, N=0, d=4096, flags=M.split_flag(32)) == M.MHC_OK        # 128 columns per CTA
     assert [M.split_flag(v) >> 8 for v in (0, 1, 2, 4, 8, 16, 32)] == [0, 1, 2, 3, 4, 5, 6]
@@ -110,11 +111,12 @@ def test_fused_validation(M):
 
 def test_split_choices(M):
     B = M.lib.mhc_packed_block_columns()
-    # d/split a multiple of 64 (whole accumulation groups) in [128, 640] for some split <= 32
-    ok = {4 * B: M.MHC_OK, 256: M.MHC_OK, 512: M.MHC_OK, 640: M.MHC_OK, 1024: M.MHC_OK,
-          2048: M.MHC_OK, 5120: M.MHC_OK, 6144: M.MHC_OK, 7168: M.MHC_OK, 20480: M.MHC_OK,
-          704: M.MHC_ERR_SHAPE, 5632: M.MHC_ERR_SHAPE, 2 * B: M.MHC_ERR_SHAPE,
-          100: M.MHC_ERR_SHAPE, 24576: M.MHC_ERR_SHAPE, 20992: M.MHC_ERR_SHAPE}
+    # d/split a multiple of 32 (whole pipeline slots) in [128, 640] for some split <= 32
+    ok = {4 * B: M.MHC_OK, 160: M.MHC_OK, 256: M.MHC_OK, 512: M.MHC_OK, 640: M.MHC_OK,
+          704: M.MHC_OK, 1024: M.MHC_OK, 2048: M.MHC_OK, 5120: M.MHC_OK, 5632: M.MHC_OK,
+          6144: M.MHC_OK, 7168: M.MHC_OK, 20480: M.MHC_OK,
+          2 * B: M.MHC_ERR_SHAPE, 100: M.MHC_ERR_SHAPE, 24576: M.MHC_ERR_SHAPE,
+          20992: M.MHC_ERR_SHAPE, 5000: M.MHC_ERR_SHAPE}
     for d, want in ok.items():
         assert _fused(M, N=0, d=d, ws_bytes=1 << 40) == want, d
 

@@ -47,6 +47,8 @@ CASES = [
     (300, 5120, 16),         # 16 CTAs per tile, 320 columns each
     (200, 8192, 16),
     (160, 4096, 32),         # 32 CTAs per tile, the narrowest slices
+    (300, 5120, 32),         # 5 slots per CTA: the last accumulation group holds one slot
+    (200, 704, 2),           # 11 slots per CTA
 ]
 
 
@@ -216,9 +218,9 @@ def test_automatic_shape_choice(M):
     for N in (256, 4096, 32768, 131072, 1000):
         split, tile, groups = M.step_config(N, 5120)
         assert tile % 8 == 0 and 8 <= tile <= 128 and tile % split == 0
-        options = [cost(N, s, t) for s in (8, 16) for t in range(128, 7, -8) if t % s == 0]
+        options = [cost(N, s, t) for s in (8, 16, 32) for t in range(128, 7, -8) if t % s == 0]
         assert cost(N, split, tile) == min(options), N
     if ctas == 152:
         assert M.step_config(32768, 5120)[:2] == (8, 128)
         assert M.step_config(4096, 5120)[:2] == (8, 112)
-        assert M.step_config(256, 5120)[:2] == (16, 32)
+        assert M.step_config(256, 5120)[:2] == (32, 64)

@@ -1,12 +1,17 @@
-"""The fused step on host-resident tensors (mhc_fused_step_host): chunks through two staging
+"""The fused step on host-resident tensors (mhc_fused_step_host): chunks through the staging
 slots on three streams give, token for token, the device step's results and the oracle's, for
 ragged last chunks, chunk sizes that are not a multiple of the token tile, one chunk larger than
-the batch, an in-place host update, and a caller stream other than the default."""
+the batch, an in-place host update, and a caller stream other than the default.
+
+A chunk may run with another launch shape (CTAs per tile) than the whole batch, which changes
+the order in which the projection's partial sums are added: X' is bit-exact whatever the shape,
+y and the mix outputs agree within the parity tolerances."""
 import numpy as np
 import pytest
 import torch
 
-from tests.parity import check_step, oracle_step
+from tests.parity import (TOL_M_REL, TOL_PUC, assert_abs, assert_bf16_within, assert_exact,
+                          assert_mixes, check_step, oracle_step, to64)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -38,6 +43,19 @@ def _host_step(M, inp, h, stream=None, **kw):
     return o
 
 
+def _same_step(got, want):
+    """X' bit-exact; y within 2 bf16 ulps; p, u, C and m within the parity tolerances."""
+    assert set(got) == set(want)
+    for k in want:
+        assert got[k].device.type == "cpu"
+    assert_exact(to64(got["Xp"]), to64(want["Xp"]), "X'")
+    assert_bf16_within(to64(got["y"]), to64(want["y"]))
+    for k in ("pre", "post", "comb"):
+        assert_abs(to64(got[k]), to64(want[k]), TOL_PUC, k)
+    if "mixes" in want:
+        assert_mixes(to64(got["mixes"]), to64(want["mixes"]), TOL_M_REL)
+
+
 def _device_step(M, inp, with_mixes):
     o = M.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], inp["W"],
                      inp["scale"], inp["base"], inp["gain"], with_mixes=with_mixes)
@@ -59,10 +77,7 @@ def test_host_pipeline_matches_device_step(M, synth, N, d, chunk, with_mixes):
     got = _host_step(M, inp, h, chunk_tokens=chunk, with_mixes=with_mixes)
     assert M.get_status() == M.MHC_OK
     want = _device_step(M, inp, with_mixes)
-    assert set(got) == set(want)
-    for k in want:
-        assert got[k].device.type == "cpu"
-        assert torch.equal(got[k], want[k]), k
+    _same_step(got, want)
 
 
 def test_host_pipeline_oracle_parity_side_stream(M, synth):
@@ -82,8 +97,7 @@ def test_host_pipeline_in_place(M, synth):
     X_host = h["X"]
     got = _host_step(M, inp, h, chunk_tokens=200, out={"Xp": X_host})
     assert got["Xp"].data_ptr() == X_host.data_ptr()
-    for k in want:
-        assert torch.equal(got[k], want[k]), k
+    _same_step(got, want)
 
 
 def test_host_pipeline_repeated_calls_reuse_staging(M, synth):
@@ -94,8 +108,7 @@ def test_host_pipeline_repeated_calls_reuse_staging(M, synth):
         h = _host_inputs(inp)
         got = _host_step(M, inp, h, chunk_tokens=128, staging=stg)
         want = _device_step(M, inp, False)
-        for k in want:
-            assert torch.equal(got[k], want[k]), (seed, k)
+        _same_step(got, want)
     with pytest.raises(M.MhcError):
         M.fused_step_host(h["X"], h["F"], h["pre"], h["post"], h["comb"], inp["W"], inp["scale"],
                           inp["base"], inp["gain"], chunk_tokens=256, staging=stg)
