@@ -42,43 +42,53 @@
 namespace mhc {
 namespace {
 
-constexpr int TT = STEP_TT;
-constexpr int DC = STEP_DC;             // columns per X/F slot (128-byte rows)
+constexpr int TT = STEP_TT;             // token rows of a tile (at most)
+constexpr int MMA_M = 128;              // the MMA's M: A and D rows at and past the tile are ignored
+constexpr int DC = STEP_DC;             // columns per X/F slot
 constexpr int ROWB = STEP_ROW_BYTES;
-constexpr int WDC = STEP_WDC;           // columns per packed weight block: half a slot
-constexpr int HALVES = DC / WDC;        // weight blocks, and consumer passes, per slot
-constexpr int CPH = 2;                  // 16-byte chunks per consumer thread per pass
+constexpr int WDC = STEP_WDC;           // columns per packed weight block
+constexpr int HALVES = DC / WDC;        // weight blocks per slot
 constexpr int KSTEPS = WDC / 16;        // MMA K-steps per stream per weight block
 constexpr int PG = 16 / (4 * HALVES * KSTEPS);      // slots per accumulation group (16 MMAs)
-constexpr int NSTAGE = DC == 32 ? 4 : 2;            // X/F ring depth (40 or 80 KB slots)
+constexpr int NSTAGE = 4;               // X/F ring depth (40 KB slots)
 constexpr int NW = 2;                   // weight ring entries (one block each)
 // slots by which the y_hat stash ring outlasts a tile: the previous tile's RMS factor is taken
 // after slot RLAG - 1 and used from slot RLAG on
-constexpr int RLAG = DC == 32 ? 2 : 1;
+constexpr int RLAG = 2;
 constexpr int NCONS = 8;                // consumer warps (2 per TMEM lane quarter)
 constexpr int NROLE = 2;                // warp 0: TMA producer; warp 1: TMEM owner and MMA issuer
 constexpr int STORE_WARP = NROLE + NCONS;           // warp 10: X'/y TMA stores
 constexpr int FIN_WARP = STORE_WARP + 1;            // warp 11: scale, split, Sinkhorn
 constexpr int NTHREADS = (FIN_WARP + 1) * 32;
-static_assert(2 * HALVES * CPH == STEP_CHUNKS, "2 thread halves x passes x chunks cover a row");
+// Consumer layout: TT tokens over the TT/32 lane quarters whose TMEM lanes hold their
+// accumulator rows; TPT threads per token (2 per quarter holding the token, times the quarters
+// that share it), each owning CPH 16-byte chunks of every row of a slot. Only the warps in the
+// quarters that hold accumulator rows fold (NFOLD warps).
+constexpr int QPT = TT / 32;
+constexpr int TPT = NCONS * 32 / TT;
+constexpr int CPH = STEP_CHUNKS / TPT;
+constexpr int NFOLD = NCONS * QPT / 4;
+static_assert(CPH == 2, "a consumer thread owns 32 bytes of each slot row");
 static_assert(4 * HALVES * KSTEPS * PG == 16, "accumulation groups of 16 MMAs");
-constexpr int TILE_BYTES = TT * ROWB;               // one [128 tokens x DC] tile: 16 KB
+constexpr int TILE_BYTES = TT * ROWB;               // one [TT tokens x DC] tile
 constexpr int STAGE_BYTES = 5 * TILE_BYTES;         // X_0..X_3 and F
 constexpr int RUN_STRIDE = 24;                      // floats per token of the local running sums
-constexpr int PART_STRIDE = 28;                     // floats per token of an exchange row
+// exchange row per token: 24 mix sums, then S_x of each of the TPT parts, then their S_y
+constexpr int PART_STRIDE = 24 + 2 * TPT;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = STEP_MMA_N;         // two accumulators, at columns 0 and 80
 constexpr uint32_t STASH_COL = 2 * ACC_COLS;
-// y_hat stash: a ring of S + RLAG slots of SLOT_COLS columns (both thread halves), so the
-// widest slice is STASH_SLOTS - RLAG slots.
-constexpr int PASS_COLS = 4 * CPH;                   // packed bf16 pairs per thread and pass
-constexpr int SLOT_COLS = 2 * HALVES * PASS_COLS;    // 32
+// y_hat stash: a ring of S + RLAG slots; each TMEM lane holds two threads' PASS_COLS columns per
+// slot, so the widest slice is STASH_SLOTS - RLAG slots.
+constexpr int PASS_COLS = 4 * CPH;                   // packed bf16 pairs per thread and slot
+constexpr int SLOT_COLS = 2 * PASS_COLS;
 constexpr int STASH_SLOTS = static_cast<int>(TMEM_COLS - STASH_COL) / SLOT_COLS;
-constexpr int MAX_SLICE = (STASH_SLOTS - RLAG) * DC;    // 640 columns
+constexpr int MAX_SLICE = (STASH_SLOTS - RLAG) * DC;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s
 constexpr uint64_t DEBUG_WAIT_NS = 2000000ull;           // 2 ms
 
 constexpr int PART_BYTES = TT * PART_STRIDE * 4;   // one tile's exchange rows (global scratch)
+static_assert(PART_STRIDE % 4 == 0, "exchange rows of whole float4s");
 constexpr int RUN_BYTES = TT * RUN_STRIDE * 4;     // one tile's running sums; two of them
 constexpr int OFF_W = NSTAGE * STAGE_BYTES;
 constexpr int OFF_PART = OFF_W + NW * STEP_WBLOCK_BYTES;
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // u % HALVES of slot u / HALVES) goes to entry u % NW, and an entry is refilled with block
     // u + NW once the MMAs that read block u have completed. The X/F producer never waits on it.
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(TT, STEP_MMA_N);
+      constexpr uint32_t idesc = idesc_bf16_f32(MMA_M, STEP_MMA_N);
       const uint64_t weight_pol = policy_evict_last();
       const int nblocks = ((ntiles - c0 + nclust - 1) / nclust) * S * HALVES;
       auto load_block = [&](int u) {
@@ -369,22 +379,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ------------------------------------------------------------------ consumers
     const int c = warp - NROLE;
     const int sub = warp & 3;           // TMEM lane quarter this warp may access
-    const int h = c >> 2;               // which half of a slot's columns, which 12 mix numbers
-    const int tl = sub * 32 + lane;     // token row within a tile
+    const int h = c >> 2;               // which of the quarter's two warps; a folder's 12 mix numbers
+    const int tl = (sub % QPT) * 32 + lane;             // token row within a tile
+    const int part = (sub / QPT) * 2 + h;               // which CPH chunks of each slot row
+    const bool folder = sub < QPT;      // its TMEM lane holds the token's accumulator row
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
-    // pass hs of this thread covers 16-byte chunks chunk0(hs) + q, q < CPH, of its token row
-    auto chunk0 = [&](int hs) { return (h * HALVES + hs) * CPH; };
-    uint32_t row_off[HALVES][CPH];
+    const int chunk0 = part * CPH;      // this thread's 16-byte chunks: chunk0 + q, q < CPH
+    uint32_t row_off[CPH];
 #pragma unroll
-    for (int hs = 0; hs < HALVES; ++hs)
-#pragma unroll
-      for (int q = 0; q < CPH; ++q) row_off[hs][q] = tile_chunk_offset(tl, chunk0(hs) + q);
-    // the y_hat stash: a ring of R slots; global slot gs uses ring slot gs % R, pass hs of this
-    // thread half its PASS_COLS columns at hs * PASS_COLS
-    const uint32_t stash = lane_base + STASH_COL + static_cast<uint32_t>(h * R * HALVES * PASS_COLS);
-    auto slot_addr = [&](int slot, int hs) {
-      return stash + static_cast<uint32_t>((slot * HALVES + hs) * PASS_COLS);
-    };
+    for (int q = 0; q < CPH; ++q) row_off[q] = tile_chunk_offset(tl, chunk0 + q);
+    // the y_hat stash, in this thread's own TMEM lane: a ring of R slots of PASS_COLS columns;
+    // global slot gs uses ring slot gs % R
+    const uint32_t stash = lane_base + STASH_COL + static_cast<uint32_t>(h * R * PASS_COLS);
+    auto slot_addr = [&](int slot) { return stash + static_cast<uint32_t>(slot * PASS_COLS); };
 
     f2 cu[4], cc[4][4], cp[4];
     auto load_coeffs = [&](int tile) {
@@ -413,7 +420,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto rms_factor = [&](int it_) {
       const unsigned target = static_cast<unsigned>(((it_ >> 1) + 1) * split * NCONS);
       if (!gwait(&syready[it_ & 1], target, limit())) timed_out = true;
-      // S_y of both halves of every rank's row, eight ranks' loads in flight at a time
+      // S_y of every part of every rank's row, eight ranks' loads in flight at a time
       float sy = 0.f;
       for (int rk0 = 0; rk0 < split; rk0 += 8) {
         float v[8];
@@ -421,8 +428,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int u = 0; u < 8; ++u) {
           v[u] = 0.f;
           if (rk0 + u < split) {
-            const float2 q2 = __ldcg(reinterpret_cast<const float2*>(gpart(it_ & 1, rk0 + u) + tl * PART_STRIDE + 26));
-            v[u] = q2.x + q2.y;
+            const float* row = gpart(it_ & 1, rk0 + u) + tl * PART_STRIDE + 24 + TPT;
+            if constexpr (TPT == 4) {
+              const float4 q4 = __ldcg(reinterpret_cast<const float4*>(row));
+              v[u] = (q4.x + q4.y) + (q4.z + q4.w);
+            } else {
+              const float2 q2 = __ldcg(reinterpret_cast<const float2*>(row));
+              v[u] = q2.x + q2.y;
+            }
           }
         }
         sy += ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
@@ -477,7 +490,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // store warp writes it out with this slot's X'
         const bool consume = FUSED && gs >= R;
         uint32_t prev[PASS_COLS];
-        if (consume) stash_load_nowait(slot_addr(slot, 0), prev);
+        if (consume) stash_load_nowait(slot_addr(slot), prev);
         if (!mbar_wait(&full[b], (gs / NSTAGE) & 1, limit())) timed_out = true;
         if (consume) tmem_ld_wait();
         f2 lx{0.f, 0.f};   // this slot's sum of squares, added to the running sum once
@@ -485,31 +498,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const f2 r_src = s >= RLAG ? r_new : r_old;
           const int ycol = col0 + (s >= RLAG ? s - RLAG : s + S - RLAG) * cstride;   // slot of gs - R
           f2 ly{0.f, 0.f};
-#pragma unroll
-          for (int hs = 0; hs < HALVES; ++hs) {
-            if (consume && hs > 0) stash_load(slot_addr(slot, hs), prev);
+          {
             uint32_t ywall[PASS_COLS];
 #pragma unroll
             for (int q = 0; q < CPH; ++q) {
               uint32_t xw[4][4], fw[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[hs][q]);
+                const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[q]);
                 xw[k][0] = v.x;
                 xw[k][1] = v.y;
                 xw[k][2] = v.z;
                 xw[k][3] = v.w;
               }
               {
-                const uint4 v = *reinterpret_cast<const uint4*>(sm + ftile(b) + row_off[hs][q]);
+                const uint4 v = *reinterpret_cast<const uint4*>(sm + ftile(b) + row_off[q]);
                 fw[0] = v.x;
                 fw[1] = v.y;
                 fw[2] = v.z;
                 fw[3] = v.w;
               }
               if (consume) {
-                *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[hs][q]) =
-                    rms_scale8(prev + 4 * q, P.gain, ycol + (chunk0(hs) + q) * 8, r_src);
+                *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[q]) =
+                    rms_scale8(prev + 4 * q, P.gain, ycol + (chunk0 + q) * 8, r_src);
               }
               uint32_t ow[4][4];
 #pragma unroll
@@ -540,10 +551,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4*>(sm + xtile(b, k) + row_off[hs][q]) =
+                *reinterpret_cast<uint4*>(sm + xtile(b, k) + row_off[q]) =
                     make_uint4(ow[k][0], ow[k][1], ow[k][2], ow[k][3]);
             }
-            stash_store(slot_addr(slot, hs), ywall);
+            stash_store(slot_addr(slot), ywall);
           }
           sy2 = add2(sy2, ly);
           fence_proxy_async_smem();
@@ -551,18 +562,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (lane == 0) mbar_arrive(&xready[b]);
         } else {
 #pragma unroll
-          for (int hs = 0; hs < HALVES; ++hs) {
+          for (int q = 0; q < CPH; ++q) {
 #pragma unroll
-            for (int q = 0; q < CPH; ++q) {
+            for (int k = 0; k < 4; ++k) {
+              const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[q]);
+              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint4 v = *reinterpret_cast<const uint4*>(sm + xtile(b, k) + row_off[hs][q]);
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                  const f2 x = bf2_to_f2(wv[w]);
-                  lx = fma2(x, x, lx);
-                }
+              for (int w = 0; w < 4; ++w) {
+                const f2 x = bf2_to_f2(wv[w]);
+                lx = fma2(x, x, lx);
               }
             }
           }
@@ -574,7 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // Fold group q in the last slot of group q+1 (global numbering, across tiles): the MMA
         // that reuses q's accumulator (group q+2) starts only after this warp's xready of a
         // later slot.
-        if ((s % PG == PG - 1 || s == S - 1) && it * G + s / PG >= 1) fold(folded++);
+        if (folder && (s % PG == PG - 1 || s == S - 1) && it * G + s / PG >= 1) fold(folded++);
         // the previous tile's RMS factor, needed from slot RLAG on: fetched after slot RLAG-1's
         // work is published, so the wait overlaps that slot's MMAs and stores
         if (FUSED && s == RLAG - 1 && it > 0) r_new = rms_factor(it - 1);
@@ -583,14 +591,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (tr && warp == NROLE && lane == 0) tr[2] = global_timer_ns() - tr[0];
 
       // ------------------------------------------------------------ post this slice's sums
-      // row layout: [0..23] mix sums (half h owns 12h..12h+11), [24 + h] S_x, [26 + h] S_y.
+      // row layout: [0..23] mix sums (folder half h owns 12h..12h+11), [24 + part] S_x,
+      // [24 + TPT + part] S_y.
       // The group buffer it & 1 was last read (by every finisher) two tiles ago.
       if (it >= 2 && !gwait(&pfree[it & 1], static_cast<unsigned>((it >> 1) * split), limit()))
         timed_out = true;
       {
         float* pt = gpart(it & 1, g) + tl * PART_STRIDE;
-        pt[24 + h] = sx2.x + sx2.y;
-        pt[26 + h] = sy2.x + sy2.y;
+        pt[24 + part] = sx2.x + sx2.y;
+        pt[24 + TPT + part] = sy2.x + sy2.y;
       }
       __syncwarp();
       if (FUSED && lane == 0) gcount_release(&syready[it & 1]);
@@ -600,7 +609,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---------------------------------------------------------------- after the last tile
     const int ngroups_total = it * G;
-    while (folded < ngroups_total) fold(folded++);
+    while (folder && folded < ngroups_total) fold(folded++);
     if (FUSED && it > 0) {
       // y still in the stash: the last R global slots (tile it-1's slots and, before them, the
       // last RLAG slots of tile it-2)
@@ -613,15 +622,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int g1 = std::min(gs, g0 + NYSLOTS);
         for (int src = g0; src < g1; ++src) {
           const f2 r = (src / S == it - 1) ? r_last : r_before;
+          uint32_t w[PASS_COLS];
+          stash_load(slot_addr(src % R), w);
 #pragma unroll
-          for (int hs = 0; hs < HALVES; ++hs) {
-            uint32_t w[PASS_COLS];
-            stash_load(slot_addr(src % R, hs), w);
-#pragma unroll
-            for (int q = 0; q < CPH; ++q)
-              *reinterpret_cast<uint4*>(sm + yslot(src - g0) + row_off[hs][q]) =
-                  rms_scale8(w + 4 * q, P.gain, col0 + (src % S) * cstride + (chunk0(hs) + q) * 8, r);
-          }
+          for (int q = 0; q < CPH; ++q)
+            *reinterpret_cast<uint4*>(sm + yslot(src - g0) + row_off[q]) =
+                rms_scale8(w + 4 * q, P.gain, col0 + (src % S) * cstride + (chunk0 + q) * 8, r);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, NCONS * 32);
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int it = 0;
     for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
       const int pb = it & 1;
-      if (!gwait(&pready[pb], static_cast<unsigned>(((it >> 1) + 1) * split * NCONS), limit()))
+      if (!gwait(&pready[pb], static_cast<unsigned>(((it >> 1) + 1) * split * NFOLD), limit()))
         timed_out = true;
       const int t0 = tile * tt;
       if (per >= 8) {
@@ -681,7 +687,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               s0[u].x += v0.x; s0[u].y += v0.y; s0[u].z += v0.z; s0[u].w += v0.w;
               s1[u].x += v1.x; s1[u].y += v1.y; s1[u].z += v1.z; s1[u].w += v1.w;
               s2[u].x += v2.x; s2[u].y += v2.y; s2[u].z += v2.z; s2[u].w += v2.w;
-              s6[u].x += v6.x + v6.y;
+              s6[u].x += TPT == 4 ? (v6.x + v6.y) + (v6.z + v6.w) : v6.x + v6.y;   // S_x parts
             }
           }
           if (base_t + 16 >= per) {
@@ -720,37 +726,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int tt_ = base_t + lq;
           const bool in_range = tt_ < per;
           const int tl2 = static_cast<int>(g) * per + min(tt_, per - 1);
-          float acc[26];   // 24 mix sums, then S_x of both halves
+          constexpr int NACC = 24 + TPT;   // 24 mix sums, then the S_x parts
+          constexpr int NV = PART_STRIDE / 4;
+          float acc[NACC];
 #pragma unroll
-          for (int e = 0; e < 26; ++e) acc[e] = 0.f;
+          for (int e = 0; e < NACC; ++e) acc[e] = 0.f;
           for (int rk = lr; rk < split; rk += 2 * L) {
             const bool two = rk + L < split;
             const float4* r0 = reinterpret_cast<const float4*>(gpart(pb, rk) + tl2 * PART_STRIDE);
             const float4* r1 = reinterpret_cast<const float4*>(gpart(pb, two ? rk + L : rk) + tl2 * PART_STRIDE);
-            float4 v0[7], v1[7];
+            float4 v0[NV], v1[NV];
 #pragma unroll
-            for (int e = 0; e < 7; ++e) {
+            for (int e = 0; e < NV; ++e) {
               v0[e] = __ldcg(r0 + e);
               v1[e] = two ? __ldcg(r1 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int e = 0; e < 7; ++e) {
+            for (int e = 0; e < NV; ++e) {
               const float a4[4] = {v0[e].x + v1[e].x, v0[e].y + v1[e].y, v0[e].z + v1[e].z, v0[e].w + v1[e].w};
 #pragma unroll
               for (int c = 0; c < 4; ++c)
-                if (4 * e + c < 26) acc[4 * e + c] += a4[c];
+                if (4 * e + c < NACC) acc[4 * e + c] += a4[c];
             }
           }
           for (int off = 1; off < L; off <<= 1)
 #pragma unroll
-            for (int e = 0; e < 26; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+            for (int e = 0; e < NACC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
           if (base_t + TP >= per) {
             // every read of buffer pb is done: the group may reuse it
             __syncwarp();
             if (lane == 0) gcount_release(&pfree[pb]);
           }
           const int token2 = t0 + static_cast<int>(g) * per + tt_;
-          const float rs = __frsqrt_rn(__fdiv_rn(acc[24] + acc[25], static_cast<float>(4 * d)) + P.norm_eps);
+          float sxt = 0.f;
+#pragma unroll
+          for (int e = 24; e < NACC; ++e) sxt += acc[e];
+          const float rs = __frsqrt_rn(__fdiv_rn(sxt, static_cast<float>(4 * d)) + P.norm_eps);
           float m[24];
 #pragma unroll
           for (int e = 0; e < 24; ++e) m[e] = acc[e] * rs;

@@ -3,6 +3,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "layout.cuh"
+
 namespace mhc {
 
 // Device address of the library's status word on the current device (see mhc_get_status).
@@ -46,7 +48,7 @@ bool split_ok(int d, int split);
 // The smallest split that fits width d (or `forced` if it fits); 0 if none.
 int choose_split(int d, int forced);
 // Launch shape of the step kernel: CTAs per tile, tokens per tile (a multiple of 8 and of the
-// split, <= 128) and groups launched. `forced_*` != 0 pins a value; split 0 if nothing fits.
+// split, <= STEP_TT) and groups launched. `forced_*` != 0 pins a value; split 0 if nothing fits.
 struct StepShape {
   int split;
   int tt;
@@ -58,10 +60,11 @@ StepShape choose_shape(int64_t N, int d, int ctas, int forced_split, int forced_
 // GB300 at d = 5120, 20 slots per tile: 685 us for 256 tiles of 128 tokens, 955 us for 512
 // tiles of 64.
 constexpr int kTileCostTokens = 96;
-// Tile height forced by the flags (MHC_TILE_SHIFT bits), 0 if automatic; -1 if invalid.
+// Tile height forced by the flags (MHC_TILE_SHIFT bits), 0 if automatic; -1 if invalid (over
+// the STEP_TT rows a tile holds).
 inline int tile_flag(unsigned flags) {
   const int v = static_cast<int>((flags >> 16) & 0x1Fu);
-  return v == 0 ? 0 : (v <= 16 ? 8 * v : -1);
+  return v == 0 ? 0 : (8 * v <= STEP_TT ? 8 * v : -1);
 }
 // Split forced by the flags (MHC_SPLIT_SHIFT bits hold log2(split) + 1), 0 if automatic; -1 if
 // invalid.

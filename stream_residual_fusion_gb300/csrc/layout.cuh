@@ -7,10 +7,11 @@
 
 namespace mhc {
 
-constexpr int STEP_TT = 128;     // tokens per tile (the MMA's M)
-
-// X and F slots: STEP_DC columns of d per pipeline slot (32: 64-byte rows, a 4-deep ring of
-// 40 KB slots; 64: 128-byte rows, a 2-deep ring of 80 KB slots).
+// A pipeline slot is STEP_TT token rows of STEP_DC columns of X_0..X_3 and F: 40 KB, so four
+// slots fit in shared memory. (The kernel also builds with 64 x 64 slots, whose 128-byte rows
+// DRAM serves better; measured slower at d = 5120: every weight block then serves half as many
+// tokens, and each group walks twice the tiles.)
+constexpr int STEP_TT = 128;     // token rows per tile (the MMA's M)
 constexpr int STEP_DC = 32;
 constexpr int STEP_ROW_BYTES = STEP_DC * 2;
 constexpr int STEP_CHUNKS = STEP_ROW_BYTES / 16;         // 16-byte chunks per row
