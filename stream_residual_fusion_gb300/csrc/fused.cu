@@ -93,8 +93,9 @@ constexpr int RUN_BYTES = TT * RUN_STRIDE * 4;     // one tile's running sums; t
 constexpr int OFF_W = NSTAGE * STAGE_BYTES;
 constexpr int OFF_PART = OFF_W + NW * STEP_WBLOCK_BYTES;
 constexpr int OFF_BARS = OFF_PART + 2 * RUN_BYTES;
-// full/empty/xready per X/F slot; wfull/wempty per weight entry; accready[2]; drained; never
-constexpr int NBARS = 3 * NSTAGE + 2 * NW + 4;
+// full/empty/xready per X/F slot; wfull/wempty per weight entry; accready[2]; posted[2];
+// mposted[2]; drained; never
+constexpr int NBARS = 3 * NSTAGE + 2 * NW + 8;
 constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;   // + slack for 1 KB alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -199,7 +200,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* wfull = xready + NSTAGE;        // [NW]: the block in weight entry e has landed
   uint64_t* wempty = wfull + NW;            // [NW]: the MMAs that read weight entry e are done
   uint64_t* accready = wempty + NW;         // [2]: an accumulation group finished in buffer i
-  uint64_t* drained = accready + 2;         // the last X'/y stores have left the ring
+  uint64_t* posted = accready + 2;          // [2]: the consumer warps wrote a tile's S_x, S_y
+  uint64_t* mposted = posted + 2;           // [2]: the folding warps wrote a tile's mix sums
+  uint64_t* drained = mposted + 2;          // the last X'/y stores have left the ring
   uint64_t* never = drained + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
 
@@ -247,6 +250,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     mbar_init(&accready[0], 1);
     mbar_init(&accready[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&posted[i], NCONS);
+      mbar_init(&mposted[i], NFOLD);
+    }
     mbar_init(drained, 1);
     mbar_init(never, 1);
     fence_mbar_init();
@@ -287,6 +294,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (FUSED) tma_load_2d_hint(sm + ftile(b), &tm_f, &full[b], i0, t0, stream_pol);
         }
         if (auto tr = trace_rec(tile)) tr[1] = global_timer_ns();
+      }
+    } else if (lane == 1) {
+      // ---------------------------------------------------------------- poster
+      // Publishes the consumers' partial rows to the group: once a tile's warps have written
+      // their S_x, S_y (posted) and mix sums (mposted) and arrived on the CTA barrier, one
+      // gpu-scope release adds the warps' count to the group counter. The release waits for
+      // the writes to reach L2, which under full memory load takes microseconds; here it stalls
+      // only this lane, not the consumer warps.
+      int it = 0;
+      for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
+        if (FUSED) {
+          if (!mbar_wait(&posted[it & 1], (it >> 1) & 1, limit())) timed_out = true;
+          gcount_release_n(&syready[it & 1], NCONS);
+        }
+        if (!mbar_wait(&mposted[it & 1], (it >> 1) & 1, limit())) timed_out = true;
+        gcount_release_n(&pready[it & 1], NFOLD);
       }
     }
   } else if (warp == 1) {
@@ -460,7 +483,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         dst[1] = src[1];
         dst[2] = src[2];
         __syncwarp();
-        if (lane == 0) gcount_release(&pready[it_ & 1]);
+        if (lane == 0) mbar_arrive(&mposted[it_ & 1]);   // published by the poster (warp 0)
         if (warp == NROLE && lane == 0) {
           if (auto tr = trace_rec(c0 + it_ * nclust)) tr[3] = global_timer_ns() - tr[0];
         }
@@ -602,7 +625,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         pt[24 + TPT + part] = sy2.x + sy2.y;
       }
       __syncwarp();
-      if (FUSED && lane == 0) gcount_release(&syready[it & 1]);
+      if (FUSED && lane == 0) mbar_arrive(&posted[it & 1]);   // published by the poster (warp 0)
       load_coeffs(tile + nclust);
       if (tr && warp == NROLE && lane == 0) tr[6] = global_timer_ns() - tr[0];
     }

@@ -382,6 +382,9 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
 __device__ __forceinline__ void gcount_release(unsigned* ctr) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
+__device__ __forceinline__ void gcount_release_n(unsigned* ctr, unsigned n) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(n) : "memory");
+}
 __device__ __forceinline__ unsigned gload_acquire(const unsigned* ctr) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
