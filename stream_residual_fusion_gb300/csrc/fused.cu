@@ -613,6 +613,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (FUSED) tmem_wait_st();
       if (tr && warp == NROLE && lane == 0) tr[2] = global_timer_ns() - tr[0];
 
+      // the next tile's coefficients: loads issued now, so their latency overlaps the posting
+      load_coeffs(tile + nclust);
       // ------------------------------------------------------------ post this slice's sums
       // row layout: [0..23] mix sums (folder half h owns 12h..12h+11), [24 + part] S_x,
       // [24 + TPT + part] S_y.
@@ -626,7 +628,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       __syncwarp();
       if (FUSED && lane == 0) mbar_arrive(&posted[it & 1]);   // published by the poster (warp 0)
-      load_coeffs(tile + nclust);
       if (tr && warp == NROLE && lane == 0) tr[6] = global_timer_ns() - tr[0];
     }
 
