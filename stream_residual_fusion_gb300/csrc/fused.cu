@@ -440,29 +440,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return reinterpret_cast<float*>(sm + OFF_PART + (it_ & 1) * RUN_BYTES) + tl * RUN_STRIDE;
     };
     // RMS factor of tile iteration it_ for this token: y_hat sums of squares of every slice
-    auto rms_factor = [&](int it_) {
+    // RMS factor of tile iteration it_ for this token: y_hat sums of squares of every slice. In
+    // two halves, so the L2 latency overlaps other work: rms_issue waits for the group's count
+    // and issues the loads of the last eight ranks (earlier ranks, if any, are summed at once);
+    // rms_finish adds them up.
+    float rms_sy = 0.f, rms_v[8];
+    auto rms_issue = [&](int it_) {
       const unsigned target = static_cast<unsigned>(((it_ >> 1) + 1) * split * NCONS);
       if (!gwait(&syready[it_ & 1], target, limit())) timed_out = true;
-      // S_y of every part of every rank's row, eight ranks' loads in flight at a time
-      float sy = 0.f;
+      rms_sy = 0.f;
       for (int rk0 = 0; rk0 < split; rk0 += 8) {
-        float v[8];
+        if (rk0 > 0) rms_sy += ((rms_v[0] + rms_v[1]) + (rms_v[2] + rms_v[3])) +
+                               ((rms_v[4] + rms_v[5]) + (rms_v[6] + rms_v[7]));
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          v[u] = 0.f;
+          rms_v[u] = 0.f;
           if (rk0 + u < split) {
             const float* row = gpart(it_ & 1, rk0 + u) + tl * PART_STRIDE + 24 + TPT;
             if constexpr (TPT == 4) {
               const float4 q4 = __ldcg(reinterpret_cast<const float4*>(row));
-              v[u] = (q4.x + q4.y) + (q4.z + q4.w);
+              rms_v[u] = (q4.x + q4.y) + (q4.z + q4.w);
             } else {
               const float2 q2 = __ldcg(reinterpret_cast<const float2*>(row));
-              v[u] = q2.x + q2.y;
+              rms_v[u] = q2.x + q2.y;
             }
           }
         }
-        sy += ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
       }
+    };
+    auto rms_finish = [&]() {
+      const float sy = rms_sy + (((rms_v[0] + rms_v[1]) + (rms_v[2] + rms_v[3])) +
+                                 ((rms_v[4] + rms_v[5]) + (rms_v[6] + rms_v[7])));
       const float r = __frsqrt_rn(__fdiv_rn(sy, static_cast<float>(d)) + P.norm_eps);
       return f2{r, r};
     };
@@ -518,7 +526,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (consume) tmem_ld_wait();
         f2 lx{0.f, 0.f};   // this slot's sum of squares, added to the running sum once
         if (FUSED) {
-          const f2 r_src = s >= RLAG ? r_new : r_old;
           const int ycol = col0 + (s >= RLAG ? s - RLAG : s + S - RLAG) * cstride;   // slot of gs - R
           f2 ly{0.f, 0.f};
           {
@@ -540,10 +547,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fw[1] = v.y;
                 fw[2] = v.z;
                 fw[3] = v.w;
-              }
-              if (consume) {
-                *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[q]) =
-                    rms_scale8(prev + 4 * q, P.gain, ycol + (chunk0 + q) * 8, r_src);
               }
               uint32_t ow[4][4];
 #pragma unroll
@@ -579,6 +582,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             stash_store(slot_addr(slot), ywall);
           }
+          // the previous tile's RMS factor: its loads were issued after slot RLAG - 1
+          if (s == RLAG && it > 0) r_new = rms_finish();
+          if (consume) {
+            // y of global slot gs - R into the F tile (read above)
+            const f2 r_src = s >= RLAG ? r_new : r_old;
+#pragma unroll
+            for (int q = 0; q < CPH; ++q)
+              *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[q]) =
+                  rms_scale8(prev + 4 * q, P.gain, ycol + (chunk0 + q) * 8, r_src);
+          }
           sy2 = add2(sy2, ly);
           fence_proxy_async_smem();
           __syncwarp();
@@ -606,9 +619,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // that reuses q's accumulator (group q+2) starts only after this warp's xready of a
         // later slot.
         if (folder && (s % PG == PG - 1 || s == S - 1) && it * G + s / PG >= 1) fold(folded++);
-        // the previous tile's RMS factor, needed from slot RLAG on: fetched after slot RLAG-1's
-        // work is published, so the wait overlaps that slot's MMAs and stores
-        if (FUSED && s == RLAG - 1 && it > 0) r_new = rms_factor(it - 1);
+        // the previous tile's RMS factor, needed from slot RLAG on: its loads are issued after
+        // slot RLAG-1's work is published and summed in slot RLAG after the X' work
+        if (FUSED && s == RLAG - 1 && it > 0) rms_issue(it - 1);
       }
       if (FUSED) tmem_wait_st();
       if (tr && warp == NROLE && lane == 0) tr[2] = global_timer_ns() - tr[0];
@@ -637,7 +650,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (FUSED && it > 0) {
       // y still in the stash: the last R global slots (tile it-1's slots and, before them, the
       // last RLAG slots of tile it-2)
-      const f2 r_last = rms_factor(it - 1);
+      rms_issue(it - 1);
+      const f2 r_last = rms_finish();
       const f2 r_before = r_new;    // tile it-2's factor (computed during tile it-1)
       if (!mbar_wait(drained, 0, limit())) timed_out = true;   // the ring is idle now
       const uint64_t stream_pol = policy_evict_first();
