@@ -94,8 +94,8 @@ constexpr int OFF_W = NSTAGE * STAGE_BYTES;
 constexpr int OFF_PART = OFF_W + NW * STEP_WBLOCK_BYTES;
 constexpr int OFF_BARS = OFF_PART + 2 * RUN_BYTES;
 // full/empty/xready per X/F slot; wfull/wempty per weight entry; accready[2]; posted[2];
-// mposted[2]; drained; never
-constexpr int NBARS = 3 * NSTAGE + 2 * NW + 8;
+// mposted[2]; pfreed[2]; sygrp[2]; drained; never
+constexpr int NBARS = 3 * NSTAGE + 2 * NW + 12;
 constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;   // + slack for 1 KB alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -202,7 +202,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* accready = wempty + NW;         // [2]: an accumulation group finished in buffer i
   uint64_t* posted = accready + 2;          // [2]: the consumer warps wrote a tile's S_x, S_y
   uint64_t* mposted = posted + 2;           // [2]: the folding warps wrote a tile's mix sums
-  uint64_t* drained = mposted + 2;          // the last X'/y stores have left the ring
+  uint64_t* pfreed = mposted + 2;           // [2]: the group's finishers released an exchange buffer
+  uint64_t* sygrp = pfreed + 2;             // [2]: every rank of the group posted a tile's S_y
+  uint64_t* drained = sygrp + 2;            // the last X'/y stores have left the ring
   uint64_t* never = drained + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
 
@@ -253,6 +255,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&posted[i], NCONS);
       mbar_init(&mposted[i], NFOLD);
+      mbar_init(&pfreed[i], 1);
+      mbar_init(&sygrp[i], 1);
     }
     mbar_init(drained, 1);
     mbar_init(never, 1);
@@ -297,16 +301,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     } else if (lane == 1) {
       // ---------------------------------------------------------------- poster
-      // Publishes the consumers' partial rows to the group: once a tile's warps have written
-      // their S_x, S_y (posted) and mix sums (mposted) and arrived on the CTA barrier, one
-      // gpu-scope release adds the warps' count to the group counter. The release waits for
-      // the writes to reach L2, which under full memory load takes microseconds; here it stalls
-      // only this lane, not the consumer warps.
+      // The CTA's link to its group's counters in global memory, so that no consumer warp waits
+      // on an L2 round trip: a gpu-scope release waits for the writes to reach L2, and every
+      // acquire load of a counter is an L2 round trip too, several microseconds each under full
+      // memory load. Per tile, in order:
+      //   1. (from the third tile) wait until the group's finishers have released exchange
+      //      buffer it & 1, then tell the consumers (pfreed);
+      //   2. once the consumer warps wrote their S_x, S_y (posted), add their count to the
+      //      group's syready counter with one release;
+      //   3. wait until every rank has done so, then tell the consumers (sygrp): the tile's RMS
+      //      factors can be read;
+      //   4. once the folding warps wrote the tile's mix sums (mposted), release pready.
+      // Causality runs through this lane: the peers' release, its acquire, its CTA-scope
+      // arrive, the consumers' wait.
       int it = 0;
       for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
+        if (it >= 2) {
+          if (!gwait(&pfree[it & 1], static_cast<unsigned>((it >> 1) * split), limit()))
+            timed_out = true;
+          mbar_arrive(&pfreed[it & 1]);
+        }
         if (FUSED) {
           if (!mbar_wait(&posted[it & 1], (it >> 1) & 1, limit())) timed_out = true;
           gcount_release_n(&syready[it & 1], NCONS);
+          if (!gwait(&syready[it & 1], static_cast<unsigned>(((it >> 1) + 1) * split * NCONS), limit()))
+            timed_out = true;
+          mbar_arrive(&sygrp[it & 1]);
         }
         if (!mbar_wait(&mposted[it & 1], (it >> 1) & 1, limit())) timed_out = true;
         gcount_release_n(&pready[it & 1], NFOLD);
@@ -446,8 +466,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // rms_finish adds them up.
     float rms_sy = 0.f, rms_v[8];
     auto rms_issue = [&](int it_) {
-      const unsigned target = static_cast<unsigned>(((it_ >> 1) + 1) * split * NCONS);
-      if (!gwait(&syready[it_ & 1], target, limit())) timed_out = true;
+      // every rank posted tile it_'s S_y (seen by the poster lane)
+      if (!mbar_wait(&sygrp[it_ & 1], (it_ >> 1) & 1, limit())) timed_out = true;
       rms_sy = 0.f;
       for (int rk0 = 0; rk0 < split; rk0 += 8) {
         if (rk0 > 0) rms_sy += ((rms_v[0] + rms_v[1]) + (rms_v[2] + rms_v[3])) +
@@ -632,8 +652,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // row layout: [0..23] mix sums (folder half h owns 12h..12h+11), [24 + part] S_x,
       // [24 + TPT + part] S_y.
       // The group buffer it & 1 was last read (by every finisher) two tiles ago.
-      if (it >= 2 && !gwait(&pfree[it & 1], static_cast<unsigned>((it >> 1) * split), limit()))
-        timed_out = true;
+      if (it >= 2 && !mbar_wait(&pfreed[it & 1], ((it >> 1) - 1) & 1, limit())) timed_out = true;
       {
         float* pt = gpart(it & 1, g) + tl * PART_STRIDE;
         pt[24 + part] = sx2.x + sx2.y;
