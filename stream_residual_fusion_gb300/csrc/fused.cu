@@ -90,12 +90,17 @@ constexpr uint64_t DEBUG_WAIT_NS = 2000000ull;           // 2 ms
 constexpr int PART_BYTES = TT * PART_STRIDE * 4;   // one tile's exchange rows (global scratch)
 static_assert(PART_STRIDE % 4 == 0, "exchange rows of whole float4s");
 constexpr int RUN_BYTES = TT * RUN_STRIDE * 4;     // one tile's running sums; two of them
+// The same buffers first hold the tile's coefficients, copied in by the poster lane: post_prev
+// [TT][4], pre_prev [TT][4], comb_prev [TT][16] (96 bytes per token, as many as the sums).
+constexpr int COEF_PRE = TT * 16;
+constexpr int COEF_COMB = TT * 32;
+static_assert(COEF_COMB + TT * 64 <= RUN_BYTES, "coefficients fit a running-sum buffer");
 constexpr int OFF_W = NSTAGE * STAGE_BYTES;
 constexpr int OFF_PART = OFF_W + NW * STEP_WBLOCK_BYTES;
 constexpr int OFF_BARS = OFF_PART + 2 * RUN_BYTES;
 // full/empty/xready per X/F slot; wfull/wempty per weight entry; accready[2]; posted[2];
-// mposted[2]; pfreed[2]; sygrp[2]; drained; never
-constexpr int NBARS = 3 * NSTAGE + 2 * NW + 12;
+// mposted[2]; pfreed[2]; sygrp[2]; cfull[2]; drained; never
+constexpr int NBARS = 3 * NSTAGE + 2 * NW + 14;
 constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
 constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;   // + slack for 1 KB alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -138,10 +143,12 @@ struct StepParams {
   unsigned flags;
 };
 
-// Fold accumulation group `gg` (TMEM accumulator gg & 1) into this thread's 12 running sums.
+// Fold accumulation group `gg` (TMEM accumulator gg & 1) into this thread's 12 running sums
+// (the tile's first group sets them).
 // The packed weight rows are ordered so that half h of the 24 mix numbers, all three planes,
 // lands in accumulator columns [36h, 36h + 36): 12 hi, then 12 mid, then 12 lo.
-__device__ __forceinline__ void fold_group(uint32_t tmem_lane, int gg, int h, float* run) {
+__device__ __forceinline__ void fold_group(uint32_t tmem_lane, int gg, int h, float* run,
+                                           bool first) {
   const uint32_t col = static_cast<uint32_t>((gg & 1) * ACC_COLS + 36 * h);
   uint32_t a[32], b[4];
   tmem_ld_x32(tmem_lane + col, a);
@@ -154,7 +161,7 @@ __device__ __forceinline__ void fold_group(uint32_t tmem_lane, int gg, int h, fl
   float4* rp = reinterpret_cast<float4*>(run);
 #pragma unroll
   for (int q = 0; q < 3; ++q) {
-    float4 v = rp[q];
+    const float4 v = first ? make_float4(0.f, 0.f, 0.f, 0.f) : rp[q];
     float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -204,7 +211,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* mposted = posted + 2;           // [2]: the folding warps wrote a tile's mix sums
   uint64_t* pfreed = mposted + 2;           // [2]: the group's finishers released an exchange buffer
   uint64_t* sygrp = pfreed + 2;             // [2]: every rank of the group posted a tile's S_y
-  uint64_t* drained = sygrp + 2;            // the last X'/y stores have left the ring
+  uint64_t* cfull = sygrp + 2;              // [2]: a tile's coefficients are in its sums buffer
+  uint64_t* drained = cfull + 2;            // the last X'/y stores have left the ring
   uint64_t* never = drained + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
 
@@ -257,6 +265,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&mposted[i], NFOLD);
       mbar_init(&pfreed[i], 1);
       mbar_init(&sygrp[i], 1);
+      mbar_init(&cfull[i], 1);
     }
     mbar_init(drained, 1);
     mbar_init(never, 1);
@@ -314,6 +323,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       //   4. once the folding warps wrote the tile's mix sums (mposted), release pready.
       // Causality runs through this lane: the peers' release, its acquire, its CTA-scope
       // arrive, the consumers' wait.
+      // It also copies each tile's coefficients into the tile's running-sum buffer, one and a
+      // half tiles ahead (the buffer of tile it + 2 is free once the folders posted tile it's
+      // mix sums), so the consumers never wait on those loads at a tile start.
+      const uint64_t coef_pol = policy_evict_first();
+      auto coef_copy = [&](int it_) {
+        const int tile = c0 + it_ * nclust;
+        if (!FUSED || tile >= ntiles) return;
+        const int t0 = tile * tt;
+        const uint32_t cnt = static_cast<uint32_t>(min(tt, P.N - t0));
+        uint8_t* buf = sm + OFF_PART + (it_ & 1) * RUN_BYTES;
+        mbar_arrive_expect_tx(&cfull[it_ & 1], cnt * 96u);
+        bulk_load_hint(buf, P.post_prev + static_cast<size_t>(t0) * 4, cnt * 16u, &cfull[it_ & 1], coef_pol);
+        bulk_load_hint(buf + COEF_PRE, P.pre_prev + static_cast<size_t>(t0) * 4, cnt * 16u, &cfull[it_ & 1], coef_pol);
+        bulk_load_hint(buf + COEF_COMB, P.comb_prev + static_cast<size_t>(t0) * 16, cnt * 64u, &cfull[it_ & 1], coef_pol);
+      };
+      coef_copy(0);
+      coef_copy(1);
       int it = 0;
       for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
         if (it >= 2) {
@@ -330,6 +356,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!mbar_wait(&mposted[it & 1], (it >> 1) & 1, limit())) timed_out = true;
         gcount_release_n(&pready[it & 1], NFOLD);
+        coef_copy(it + 2);
       }
     }
   } else if (warp == 1) {
@@ -437,21 +464,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto slot_addr = [&](int slot) { return stash + static_cast<uint32_t>(slot * PASS_COLS); };
 
     f2 cu[4], cc[4][4], cp[4];
-    auto load_coeffs = [&](int tile) {
+    // this token's coefficients of tile iteration it_, from the tile's sums buffer (copied in by
+    // the poster lane)
+    auto load_coeffs = [&](int it_, int tile) {
       const int token = tile * tt + tl;
-      const bool valid = FUSED && tile < ntiles && tl < tt && token < P.N;
+      const bool valid = FUSED && tl < tt && token < P.N;
       const bool row_dest = (P.flags & 1u) != 0;
+      const float* buf = reinterpret_cast<const float*>(sm + OFF_PART + (it_ & 1) * RUN_BYTES);
+      const float* cb = buf + tl * 4;
+      const float* pb = buf + COEF_PRE / 4 + tl * 4;
+      const float* mb = buf + COEF_COMB / 4 + tl * 16;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float uk = valid ? __ldg(P.post_prev + static_cast<size_t>(token) * 4 + k) : 0.f;
-        const float pk = valid ? __ldg(P.pre_prev + static_cast<size_t>(token) * 4 + k) : 0.f;
+        const float uk = valid ? cb[k] : 0.f;
+        const float pk = valid ? pb[k] : 0.f;
         cu[k] = f2{uk, uk};
         cp[k] = f2{pk, pk};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           // cc[j][k]: coefficient of input stream j in output stream k
-          const int idx = row_dest ? (k * 4 + j) : (j * 4 + k);
-          const float v = valid ? __ldg(P.comb_prev + static_cast<size_t>(token) * 16 + idx) : 0.f;
+          const float v = valid ? mb[row_dest ? (k * 4 + j) : (j * 4 + k)] : 0.f;
           cc[j][k] = f2{v, v};
         }
       }
@@ -501,7 +533,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       const int it_ = gg / G;
       float* run = part_of(it_) + 12 * h;
-      fold_group(lane_base, gg, h, run);
+      fold_group(lane_base, gg, h, run, gg % G == 0);
       if (gg % G == G - 1) {
         // this thread's 12 mix sums of the tile are final: publish them to the group (the
         // counter's release orders what the warp wrote before __syncwarp)
@@ -510,6 +542,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         dst[0] = src[0];
         dst[1] = src[1];
         dst[2] = src[2];
+        // the sums buffer is free now: the poster's bulk copy of a later tile's coefficients
+        // will write it (async proxy after these generic accesses)
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&mposted[it_ & 1]);   // published by the poster (warp 0)
         if (warp == NROLE && lane == 0) {
@@ -517,20 +552,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     };
-    load_coeffs(c0);
 
     // RMS factors: r_old for tile it-2 (consumed in slots s < RLAG), r_new for tile it-1 (from
     // slot RLAG on; computed after slot RLAG - 1)
     f2 r_old{0.f, 0.f}, r_new{0.f, 0.f};
     int gs = 0, it = 0, folded = 0;
     int slot = 0;                        // gs % R, kept incrementally
+    // this token's coefficients of tile iteration it_, once the poster's copy has landed
+    auto take_coeffs = [&](int it_) {
+      const int tile = c0 + it_ * nclust;
+      if (!FUSED || tile >= ntiles) return;
+      if (!mbar_wait(&cfull[it_ & 1], (it_ >> 1) & 1, limit())) timed_out = true;
+      load_coeffs(it_, tile);
+    };
+    take_coeffs(0);
     for (int tile = c0; tile < ntiles; tile += nclust, ++it) {
-      float* run = part_of(it) + 12 * h;
       unsigned long long* tr = trace_rec(tile);
       if (warp == NROLE && lane == 0 && tr) tr[0] = global_timer_ns();
-      reinterpret_cast<float4*>(run)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      reinterpret_cast<float4*>(run)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      reinterpret_cast<float4*>(run)[2] = make_float4(0.f, 0.f, 0.f, 0.f);
       r_old = r_new;
 
       f2 sx2{0.f, 0.f}, sy2{0.f, 0.f};
@@ -645,9 +683,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (FUSED) tmem_wait_st();
       if (tr && warp == NROLE && lane == 0) tr[2] = global_timer_ns() - tr[0];
+      take_coeffs(it + 1);
 
-      // the next tile's coefficients: loads issued now, so their latency overlaps the posting
-      load_coeffs(tile + nclust);
       // ------------------------------------------------------------ post this slice's sums
       // row layout: [0..23] mix sums (folder half h owns 12h..12h+11), [24 + part] S_x,
       // [24 + TPT + part] S_y.
