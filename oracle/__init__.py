@@ -11,6 +11,9 @@ Pages followed (cited by title and section throughout):
   * "2A · Single-Pass mHC" -- section 3 "Giải pháp" (Sinkhorn rounds) and section 4 "Profiling"
     (the [[3,1],[1,1]] hand check and the 1e-6 float64 criterion).
 
+mx.py holds the MXFP8 encoding of y (a format the pages leave open; the reading taken is stated
+there).
+
 Every function is pinned by tests under tests/ (tests/test_oracle_*.py); nothing here is
 "parity unpinned".
 """
