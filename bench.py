@@ -498,6 +498,80 @@ def run_unfused(args):
     return 0
 
 
+# bytes per token of the step with MXFP8 y (d = 5120, n = 4): read X, F and the previous tuple;
+# write X', the E4M3 codes of y, its E8M0 block scales and p, u, C
+MXFP8_BYTES_PER_TOKEN = 5 * 5120 * 2 + 96 + 4 * 5120 * 2 + 5120 + 5120 // 32 + 96
+
+
+def run_mxfp8(args):
+    """The fused step with y written as MXFP8 (codes + block scales), timed beside the bf16-y
+    step on the same inputs (one GPU), each against its own algorithmic bytes."""
+    import torch
+    from stream_residual_fusion_gb300 import mhc, synth
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    N, d = w.N, w.d
+    inp = synth.make_workload(w, seed=3000, device=dev)
+    inp.pop("outliers", None)
+    stream = torch.cuda.current_stream(dev)
+    Wp = mhc.pack_weights(inp["W"], stream=stream)
+    scratch = torch.empty(mhc.step_scratch_bytes(d), dtype=torch.uint8, device=dev)
+    small = lambda: {"pre": torch.empty(N, 4, device=dev), "post": torch.empty(N, 4, device=dev),
+                     "comb": torch.empty(N, 4, 4, device=dev), "Xp": torch.empty_like(inp["X"])}
+    out_bf, out_mx = small(), small()
+    out_bf["y"] = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+    out_mx["y_codes"] = torch.empty(N, d, dtype=torch.uint8, device=dev)
+    out_mx["y_scale"] = torch.empty(N, d // 32, dtype=torch.uint8, device=dev)
+    args_in = (inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"])
+    tail = (inp["scale"], inp["base"], inp["gain"])
+
+    def bf16_step():
+        mhc.fused_step(*args_in, None, *tail, W_packed=Wp, scratch=scratch, out=out_bf,
+                       stream=stream)
+
+    def mx_step():
+        mhc.fused_step_mxfp8(*args_in, Wp, *tail, scratch=scratch, out=out_mx, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        bf16_step()
+        mx_step()
+    torch.cuda.synchronize()
+    K = args.steps
+    T = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [[T() for _ in range(3)] for _ in range(K)]
+    for i in range(K):                      # interleaved, so both see the same clocks
+        ev[i][0].record(stream)
+        bf16_step()
+        ev[i][1].record(stream)
+        mx_step()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if mhc.get_status() != mhc.MHC_OK:
+        raise RuntimeError("device-side wait gave up")
+    bf_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    mx_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    mx_bytes = N * MXFP8_BYTES_PER_TOKEN + 640 * d + d * 4
+    bf_bytes = algorithmic_bytes(N, d)
+    line = {
+        "metric": "fused mHC step tokens/s at n=4,d=5120 with MXFP8 y (beside the bf16-y step)",
+        "form": "mxfp8", "value": N / (mx_ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": K, "warmup": args.warmup, "ms_per_step": mx_ms, "higher_is_better": True,
+        "dtype": "bf16 streams, e4m3/e8m0 y", "data": "synthetic",
+        "config": {"workload": f"{w.name} (N={N}), n=4, d={d}", "sinkhorn_iters": 20},
+        "mxfp8_algorithmic_bytes_per_token": MXFP8_BYTES_PER_TOKEN,
+        "mxfp8_ms_p50": mx_ms, "mxfp8_frac": mx_bytes / (mx_ms / 1e3) / 1e9 / peak,
+        "bf16_ms_p50": bf_ms, "bf16_frac": bf_bytes / (bf_ms / 1e3) / 1e9 / peak,
+        "speedup_vs_bf16_y": bf_ms / mx_ms, "peak_gbs": peak, "peak_kind": peak_kind,
+        "x_prime_identical": bool(torch.equal(out_bf["Xp"], out_mx["Xp"])),
+        "gpu_launches": K * 2,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,8 +582,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of the step (no host submission cost; for small workloads)")
-    ap.add_argument("--form", choices=("fused", "unfused"), default="fused",
-                    help="unfused: time the four-kernel form beside the fused step (one GPU)")
+    ap.add_argument("--form", choices=("fused", "unfused", "mxfp8"), default="fused",
+                    help="unfused: time the four-kernel form beside the fused step; mxfp8: the "
+                         "step with MXFP8 y beside the bf16-y step (one GPU each)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="synthetic workload (default: the B=4,T=8192 prefill; others are for profiling)")
     args = ap.parse_args()
@@ -517,6 +592,8 @@ def main():
         return run_reference(args)
     if args.form == "unfused":
         return run_unfused(args)
+    if args.form == "mxfp8":
+        return run_mxfp8(args)
     return run_ours(args)
 
 

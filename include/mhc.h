@@ -126,6 +126,29 @@ int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
                           float hc_eps, float norm_eps, unsigned flags, void* scratch,
                           size_t scratch_bytes, void* stream);
 
+/* ---- the fused step with y quantised for the next sublayer ----------------------------------
+ * The pages name an FP4/FP8 MoE as a consumer of y ("2A · Single-Pass mHC", section 2, the flow
+ * diagram) but define no quantised format; this entry writes y in the OCP Microscaling (MX) v1.0
+ * format MXFP8 instead of bf16, fused into the same single pass. Everything else is as in
+ * mhc_fused_step_packed (same X', p, u, C and optional mixes, bit for bit).
+ *   y_codes  uint8 [N, d]       E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ *                                no infinities)
+ *   y_scale  uint8 [N, d / 32]  E8M0 codes: block b of token t (features 32b .. 32b + 31) has
+ *                                scale X = 2^(y_scale[t, b] - 127)
+ * The encoded values are the bf16 y that mhc_fused_step_packed returns for the same inputs (bit
+ * for bit), so the codes equal a separate MXFP8 pass over that y: X = 2^(floor(log2(amax)) - 8)
+ * with amax the block's largest |y| (code clamped to >= 0; an all-zero block takes code 0); each
+ * code is y / X rounded to the nearest E4M3 value, ties to even, saturating at +-448.
+ * Dequantised: y ~= value(code) * X.
+ * Both pointers 16-byte aligned, neither overlapping another argument.                       */
+int mhc_fused_step_mxfp8(const void* X, const void* F, const float* pre_prev,
+                         const float* post_prev, const float* comb_prev, const void* W_packed,
+                         const float* scale, const float* base, const float* gain, void* X_out,
+                         void* y_codes, void* y_scale, float* pre_out, float* post_out,
+                         float* comb_out, float* mixes_out, int64_t N, int n, int d,
+                         int sinkhorn_iters, float hc_eps, float norm_eps, unsigned flags,
+                         void* scratch, size_t scratch_bytes, void* stream);
+
 /* ---- the fused step without any allocation --------------------------------------------------
  * No counterpart in the paper: an addition for callers that cannot allocate device memory when
  * they run the step (code being captured into a CUDA graph or stream that must not allocate, a

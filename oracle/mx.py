@@ -18,10 +18,10 @@ E4M3 (the "fn" variant of the OCP FP8 formats): 1 sign bit, 4 exponent bits with
 3 mantissa bits; exponent field 0 holds subnormals m/8 * 2^-6; there are no infinities and the
 codes S.1111.111 are NaN.
 
-The decision of each code is taken from float64 y here, from float32 y in the kernel; codes may
-differ where y / X lies within float32 rounding of a boundary between two E4M3 values (and a
-scale where amax lies within it of a power of two). The parity tests compare what is unique and
-bound the rest.
+The values encoded are the bf16 y of the step (the sublayer input as the bf16 path delivers it),
+so the encoding equals a separate MXFP8 pass over that y. The oracle's bf16 y and the kernel's
+may differ by up to two bf16 ulps (the RMS statistic is summed in another order); the parity
+tests compare the codes where that cannot change a decision and bound the rest.
 """
 from __future__ import annotations
 
@@ -99,11 +99,3 @@ def mxfp8_dequantize(codes, scale) -> np.ndarray:
     N, d = codes.shape
     X = np.exp2(np.asarray(scale, dtype=np.float64) - 127.0)
     return (e4m3_decode(codes).reshape(N, d // MX_BLOCK, MX_BLOCK) * X[:, :, None]).reshape(N, d)
-
-
-def rmsnorm_f64(x, gain, eps: float) -> np.ndarray:
-    """y = gain * x / sqrt(mean(x^2) + eps) in float64, before any rounding (MoE RMSNorm, formula
-    block and Code: RMSNorm); the value the MXFP8 encoding starts from."""
-    x = np.asarray(x, dtype=np.float64)
-    r = 1.0 / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)
-    return np.asarray(gain, dtype=np.float64)[None, :] * (x * r)

@@ -71,7 +71,9 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
                  float* post_out, float* comb_out, float* mixes_out, int64_t N, int n, int d,
                  int iters, float hc_eps, float norm_eps, unsigned flags, const void* workspace,
                  uint64_t ws_bytes, void* scratch, uint64_t scratch_bytes, const float* W_mix,
-                 void* stream) {
+                 void* stream, uint8_t* y_scale = nullptr) {
+  // y_scale set: y_out receives MXFP8 E4M3 codes [N, d] (one byte each) and y_scale the E8M0
+  // block scales [N, d / 32]; otherwise y_out is bf16 [N, d].
   int split = 0;
   int rc = check_step_shape(N, n, d, iters, flags, &split);
   if (rc != MHC_OK) return rc;
@@ -86,17 +88,20 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
     if (!aligned16(p)) return MHC_ERR_ALIGN;
   if (mixes_out && !aligned16(mixes_out)) return MHC_ERR_ALIGN;
   if (W_mix && !aligned16(W_mix)) return MHC_ERR_ALIGN;
+  if (y_scale && !aligned16(y_scale)) return MHC_ERR_ALIGN;
 
   const uint64_t nt = static_cast<uint64_t>(N);
   const uint64_t K = 4ull * d;
+  const uint64_t y_bytes = nt * d * (y_scale ? 1 : 2);
   const Span ins[] = {span(X, nt * K * 2),     span(F, nt * d * 2),      span(pre_prev, nt * 16),
                       span(post_prev, nt * 16), span(comb_prev, nt * 64), span(scale, 12),
                       span(base, 96),          span(gain, 4ull * d),     span(W_mix, W_mix ? 96 * K : 0)};
-  const Span outs[] = {span(X_out, nt * K * 2), span(y_out, nt * d * 2), span(pre_out, nt * 16),
+  const Span outs[] = {span(X_out, nt * K * 2), span(y_out, y_bytes), span(pre_out, nt * 16),
                        span(post_out, nt * 16), span(comb_out, nt * 64),
                        span(mixes_out, mixes_out ? nt * 96 : 0),
                        span(workspace, workspace ? ws_bytes : 0),
-                       span(scratch, workspace ? 0 : scratch_bytes)};
+                       span(scratch, workspace ? 0 : scratch_bytes),
+                       span(y_scale, y_scale ? nt * (d / 32) : 0)};
   if (!aliasing_ok(outs, ins, 0, 0)) return MHC_ERR_ALIAS;
   if (!workspace) {  // pre-packed weights are an input too
     const Span packed_in[] = {span(W_packed, mhc_packed_weights_bytes(4, d))};
@@ -123,6 +128,7 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
   a.gain = gain;
   a.X_out = X_out;
   a.y_out = y_out;
+  a.y_scale = y_scale;
   a.pre_out = pre_out;
   a.post_out = post_out;
   a.comb_out = comb_out;
@@ -201,6 +207,20 @@ int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
                       y_out, pre_out, post_out, comb_out, mixes_out, N, n, d, sinkhorn_iters,
                       hc_eps, norm_eps, flags, nullptr, 0, scratch, scratch_bytes, nullptr,
                       stream);
+}
+
+int mhc_fused_step_mxfp8(const void* X, const void* F, const float* pre_prev,
+                         const float* post_prev, const float* comb_prev, const void* W_packed,
+                         const float* scale, const float* base, const float* gain, void* X_out,
+                         void* y_codes, void* y_scale, float* pre_out, float* post_out,
+                         float* comb_out, float* mixes_out, int64_t N, int n, int d,
+                         int sinkhorn_iters, float hc_eps, float norm_eps, unsigned flags,
+                         void* scratch, size_t scratch_bytes, void* stream) {
+  if (N > 0 && !y_scale) return MHC_ERR_NULL;
+  return fused_common(X, F, pre_prev, post_prev, comb_prev, W_packed, scale, base, gain, X_out,
+                      y_codes, pre_out, post_out, comb_out, mixes_out, N, n, d, sinkhorn_iters,
+                      hc_eps, norm_eps, flags, nullptr, 0, scratch, scratch_bytes, nullptr,
+                      stream, static_cast<uint8_t*>(y_scale));
 }
 
 int mhc_mixes(const void* X, const float* W_mix, const float* scale, const float* base,

@@ -31,6 +31,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cuda_fp8.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -69,6 +71,7 @@ constexpr int TPT = NCONS * 32 / TT;
 constexpr int CPH = STEP_CHUNKS / TPT;
 constexpr int NFOLD = NCONS * QPT / 4;
 static_assert(CPH == 2, "a consumer thread owns 32 bytes of each slot row");
+static_assert(TPT == 2 && DC == 32, "MXFP8 y: a slot row is one 32-feature block, two threads");
 static_assert(4 * HALVES * KSTEPS * PG == 16, "accumulation groups of 16 MMAs");
 constexpr int TILE_BYTES = TT * ROWB;               // one [TT tokens x DC] tile
 constexpr int STAGE_BYTES = 5 * TILE_BYTES;         // X_0..X_3 and F
@@ -102,7 +105,9 @@ constexpr int OFF_BARS = OFF_PART + 2 * RUN_BYTES;
 // mposted[2]; pfreed[2]; sygrp[2]; cfull[2]; drained; never
 constexpr int NBARS = 3 * NSTAGE + 2 * NW + 14;
 constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
-constexpr int SMEM_BYTES = OFF_TMEM + 16 + 1024;   // + slack for 1 KB alignment
+// MXFP8 y: each thread's block-maximum exponent for its partner, [2 slot parities][2 parts][TT]
+constexpr int OFF_XCH = OFF_TMEM + 16;
+constexpr int SMEM_BYTES = OFF_XCH + 4 * TT + 1024;   // + slack for 1 KB alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0 && STEP_WBLOCK_BYTES % 1024 == 0, "tile alignment");
 
@@ -114,6 +119,7 @@ __host__ __device__ constexpr int wtile(int e, int k) {
 // y staging at the very end reuses the X/F tiles of the idle ring: slot j -> stage j/5, tile j%5.
 __host__ __device__ constexpr int yslot(int j) { return (j / 5) * STAGE_BYTES + (j % 5) * TILE_BYTES; }
 constexpr int NYSLOTS = 5 * NSTAGE;
+constexpr int EB = 4;                   // stash slots the epilogue loads per TMEM wait
 
 struct StepParams {
   const float* pre_prev;
@@ -127,6 +133,7 @@ struct StepParams {
   float* post_out;
   float* comb_out;
   float* mixes_out;
+  uint8_t* y_scale;            // MXFP8 y only: E8M0 block scales [N, d / 32]
   unsigned* status;
   unsigned long long* trace;   // optional: 8 phase timestamps per (tile, CTA) (mhc_set_trace)
   unsigned* counters;          // per group: syready[2], pready[2], pfree[2] (zeroed per launch)
@@ -184,6 +191,74 @@ __device__ __forceinline__ uint4 rms_scale8(const uint32_t* w, const float* __re
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// MXFP8 y (OCP Microscaling formats v1.0: E4M3 elements, blocks of 32 features of a token that
+// share one E8M0 scale 2^(floor(log2 amax) - 8)), encoded from the bf16 y: the codes equal an
+// MXFP8 pass over the y that the bf16 path writes. A slot row is one block; each of the token's
+// two consumer threads holds 16 of its features.
+// This thread's 16 bf16 y values, packed in pairs: those of the bf16 path.
+__device__ __forceinline__ void y_bf16x16(const uint32_t* w, const float* __restrict__ gain,
+                                          int col, f2 r2, uint32_t* y) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint4 v = rms_scale8(w + 4 * q, gain, col + 8 * q, r2);
+    y[4 * q] = v.x;
+    y[4 * q + 1] = v.y;
+    y[4 * q + 2] = v.z;
+    y[4 * q + 3] = v.w;
+  }
+}
+// Biased exponent of the largest |y| of 16 bf16 values (0 for zeros and subnormals):
+// floor(log2 amax) + 127. Non-negative bf16 bit patterns order like their values.
+__device__ __forceinline__ uint32_t amax_exponent16(const uint32_t* y) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m = max(m, max(y[k] & 0x7fffu, (y[k] >> 16) & 0x7fffu));
+  return m >> 7;
+}
+// E8M0 code of a block whose largest magnitude has biased exponent e: floor(log2 amax) - 8 + 127,
+// at least 0 (an all-zero block takes 0).
+__device__ __forceinline__ uint32_t mx_scale_code(uint32_t e) { return e > 8 ? e - 8 : 0; }
+// 16 bf16 values divided by the block scale 2^(code - 127) (a power of two: exact) and rounded to
+// E4M3, nearest even, saturating at +-448; bytes in feature order.
+__device__ __forceinline__ uint4 mx_encode16(const uint32_t* y, uint32_t code) {
+  const float inv = __uint_as_float((254u - code) << 23);   // 2^(127 - code)
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t p0 = y[2 * i], p1 = y[2 * i + 1];       // features 4i, 4i+1 | 4i+2, 4i+3
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(__uint_as_float(p0 << 16) * inv, __uint_as_float(p0 & 0xffff0000u) * inv),
+        __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(__uint_as_float(p1 << 16) * inv, __uint_as_float(p1 & 0xffff0000u) * inv),
+        __NV_SATFINITE, __NV_E4M3);
+    w[i] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Staging of one slot of E4M3 codes in shared memory: the codes of tile quarter q (tokens
+// 32q .. 32q + 31, held by one pair of consumer warps) fill the first kilobyte of the 2 KB
+// at base + 2048 q, [32 rows][32 bytes] with the 32-byte swizzle, so that each pair writes only
+// bytes that it alone read before. One TMA store per full quarter (32-row boxes), 8-row boxes
+// for the rows of a partial last quarter.
+__device__ __forceinline__ uint32_t code_offset(int tl, int part) {
+  return static_cast<uint32_t>((tl >> 5) * 2048) + swizzled_chunk_offset(tl & 31, part, 32);
+}
+__device__ __forceinline__ void store_codes(const CUtensorMap* m32, const CUtensorMap* m8,
+                                            const uint8_t* base, int col, int row0, int rows,
+                                            uint64_t pol) {
+  for (int q = 0; 32 * q < rows; ++q) {
+    const int n = min(32, rows - 32 * q);
+    if (n == 32) {
+      tma_store_2d_hint(m32, base + 2048 * q, col, row0 + 32 * q, pol);
+    } else {
+      for (int j = 0; j < n; j += 8)
+        tma_store_2d_hint(m8, base + 2048 * q + 32 * j, col, row0 + 32 * q + j, pol);
+    }
+  }
+}
+
 // One pass's y_hat (PASS_COLS packed bf16 pairs) to or from the TMEM stash.
 __device__ __forceinline__ void stash_load(uint32_t taddr, uint32_t (&w)[PASS_COLS]) { tmem_ld_x8(taddr, w); }
 __device__ __forceinline__ void stash_load_nowait(uint32_t taddr, uint32_t (&w)[PASS_COLS]) {
@@ -193,11 +268,12 @@ __device__ __forceinline__ void stash_store(uint32_t taddr, const uint32_t (&w)[
 
 // Persistent: group c of gridDim.x / split groups handles tiles c, c + #groups, ... The TMA ring,
 // the accumulation groups and the barrier phases run on across tiles.
-template <bool FUSED>
+// FUSED: the whole step (else the mix numbers of X alone); MX: y as MXFP8 codes and scales.
+template <bool FUSED, bool MX = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     step_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_f,
                 const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_y,
-                const StepParams P) {
+                const __grid_constant__ CUtensorMap tm_y8, const StepParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -436,7 +512,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // the y the consumers normalised into the F tile: global slot gs - R
             const int src = gs - R;
             const int ytile = c0 + (src / S) * nclust;
-            tma_store_2d_hint(&tm_y, sm + ftile(b), col0 + (src % S) * cstride, ytile * tt, stream_pol);
+            if constexpr (MX)
+              store_codes(&tm_y, &tm_y8, sm + ftile(b), col0 + (src % S) * cstride, ytile * tt, tt, stream_pol);
+            else
+              tma_store_2d_hint(&tm_y, sm + ftile(b), col0 + (src % S) * cstride, ytile * tt, stream_pol);
           }
           bulk_commit();
           bulk_wait_read<0>();          // the slot's tiles have been read: free the slot
@@ -570,6 +649,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       unsigned long long* tr = trace_rec(tile);
       if (warp == NROLE && lane == 0 && tr) tr[0] = global_timer_ns();
       r_old = r_new;
+      // tokens of the y written in this tile's slots: tile it-1's from slot RLAG on, before that
+      // tile it-2's
+      const int ytok1 = (tile - nclust) * tt + tl, ytok2 = (tile - 2 * nclust) * tt + tl;
 
       f2 sx2{0.f, 0.f}, sy2{0.f, 0.f};
       for (int s = 0; s < S; ++s, ++gs) {
@@ -645,10 +727,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (consume) {
             // y of global slot gs - R into the F tile (read above)
             const f2 r_src = s >= RLAG ? r_new : r_old;
+            if constexpr (MX) {
+              // the block's scale needs the partner thread's maximum (the other warp of this
+              // TMEM quarter); after their barrier both have also read their F rows, which then
+              // take the quarter's codes (code_offset)
+              uint32_t yv[8];
+              y_bf16x16(prev, P.gain, ycol + chunk0 * 8, r_src, yv);
+              const uint32_t e_own = amax_exponent16(yv);
+              uint8_t* xch = sm + OFF_XCH + (gs & 1) * (2 * TT);
+              xch[part * TT + tl] = static_cast<uint8_t>(e_own);
+              named_bar_sync(3 + sub, 64);   // the quarter's two warps (ids 3..6)
+              const uint32_t code = mx_scale_code(max(e_own, static_cast<uint32_t>(xch[(part ^ 1) * TT + tl])));
+              *reinterpret_cast<uint4*>(sm + ftile(b) + code_offset(tl, part)) = mx_encode16(yv, code);
+              const int token = s >= RLAG ? ytok1 : ytok2;
+              if (part == 0 && tl < tt && token < P.N)
+                P.y_scale[static_cast<size_t>(token) * (P.d / 32) + ycol / 32] = static_cast<uint8_t>(code);
+            } else {
 #pragma unroll
-            for (int q = 0; q < CPH; ++q)
-              *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[q]) =
-                  rms_scale8(prev + 4 * q, P.gain, ycol + (chunk0 + q) * 8, r_src);
+              for (int q = 0; q < CPH; ++q)
+                *reinterpret_cast<uint4*>(sm + ftile(b) + row_off[q]) =
+                    rms_scale8(prev + 4 * q, P.gain, ycol + (chunk0 + q) * 8, r_src);
+            }
           }
           sy2 = add2(sy2, ly);
           fence_proxy_async_smem();
@@ -714,21 +813,64 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int first = std::max(0, gs - R);
       for (int g0 = first; g0 < gs; g0 += NYSLOTS) {
         const int g1 = std::min(gs, g0 + NYSLOTS);
-        for (int src = g0; src < g1; ++src) {
-          const f2 r = (src / S == it - 1) ? r_last : r_before;
-          uint32_t w[PASS_COLS];
-          stash_load(slot_addr(src % R), w);
+        if constexpr (MX) {
+          // EB stash slots per TMEM wait (the bf16 loop below measured faster one at a time).
+          // As in the main loop, the block maxima go through the spare kilobyte of each staged
+          // slot's quarter: one pair barrier per EB slots.
+          for (int b0 = g0; b0 < g1; b0 += EB) {
+            uint32_t w[EB][PASS_COLS];
 #pragma unroll
-          for (int q = 0; q < CPH; ++q)
-            *reinterpret_cast<uint4*>(sm + yslot(src - g0) + row_off[q]) =
-                rms_scale8(w + 4 * q, P.gain, col0 + (src % S) * cstride + (chunk0 + q) * 8, r);
+            for (int e = 0; e < EB; ++e)
+              if (b0 + e < g1) stash_load_nowait(slot_addr((b0 + e) % R), w[e]);
+            tmem_ld_wait();
+            uint32_t yv[EB][8], e_own[EB];
+#pragma unroll
+            for (int e = 0; e < EB; ++e) {
+              const int src = b0 + e;
+              if (src < g1) {
+                const f2 r = (src / S == it - 1) ? r_last : r_before;
+                y_bf16x16(w[e], P.gain, col0 + (src % S) * cstride + chunk0 * 8, r, yv[e]);
+                e_own[e] = amax_exponent16(yv[e]);
+                sm[yslot(src - g0) + sub * 2048 + 1024 + part * 32 + lane] = static_cast<uint8_t>(e_own[e]);
+              }
+            }
+            named_bar_sync(3 + sub, 64);
+#pragma unroll
+            for (int e = 0; e < EB; ++e) {
+              const int src = b0 + e;
+              if (src < g1) {
+                const uint32_t other = sm[yslot(src - g0) + sub * 2048 + 1024 + (part ^ 1) * 32 + lane];
+                const uint32_t code = mx_scale_code(max(e_own[e], other));
+                *reinterpret_cast<uint4*>(sm + yslot(src - g0) + code_offset(tl, part)) = mx_encode16(yv[e], code);
+                const int token = (c0 + (src / S) * nclust) * tt + tl;
+                if (part == 0 && tl < tt && token < P.N)
+                  P.y_scale[static_cast<size_t>(token) * (P.d / 32) + (col0 + (src % S) * cstride) / 32] =
+                      static_cast<uint8_t>(code);
+              }
+            }
+          }
+        } else {
+          for (int src = g0; src < g1; ++src) {
+            const f2 r = (src / S == it - 1) ? r_last : r_before;
+            uint32_t w[PASS_COLS];
+            stash_load(slot_addr(src % R), w);
+            const int col = col0 + (src % S) * cstride;
+#pragma unroll
+            for (int q = 0; q < CPH; ++q)
+              *reinterpret_cast<uint4*>(sm + yslot(src - g0) + row_off[q]) =
+                  rms_scale8(w + 4 * q, P.gain, col + (chunk0 + q) * 8, r);
+          }
         }
         fence_proxy_async_smem();
         named_bar_sync(1, NCONS * 32);
         if (warp == NROLE && lane == 0) {
           for (int src = g0; src < g1; ++src) {
             const int ytile = c0 + (src / S) * nclust;
-            tma_store_2d_hint(&tm_y, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, stream_pol);
+            if constexpr (MX)
+              store_codes(&tm_y, &tm_y8, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, tt,
+                          stream_pol);
+            else
+              tma_store_2d_hint(&tm_y, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, stream_pol);
           }
           bulk_commit();
           bulk_wait_read<0>();
@@ -945,6 +1087,20 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
+// MXFP8 codes of y [N, d], one byte each: boxes of DC bytes x box_rows, 32-byte swizzle.
+bool map_codes(CUtensorMap* m, const void* p, int64_t N, int d, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N)};
+  const cuuint64_t str[1] = {static_cast<cuuint64_t>(d)};
+  const cuuint32_t box[2] = {DC, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(p), dims, str, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool map_streams(CUtensorMap* m, const void* p, int64_t N, int d, uint32_t box_rows) {   // [N, 4, d]
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), 4, static_cast<cuuint64_t>(N)};
   const cuuint64_t str[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 8};
@@ -962,8 +1118,8 @@ bool map_rows(CUtensorMap* m, const void* p, int64_t rows, int64_t cols, uint32_
 // CTAs of the step kernel the current device holds at once (one per SM).
 template <typename Kern>
 cudaError_t resident_ctas(Kern kern, int* ctas) {
-  static int cache[2] = {0, 0};
-  const int which = (kern == step_kernel<true>) ? 1 : 0;
+  static int cache[3] = {0, 0, 0};
+  const int which = (kern == step_kernel<true>) ? 1 : (kern == step_kernel<true, true>) ? 2 : 0;
   if (cache[which] > 0) {
     *ctas = cache[which];
     return cudaSuccess;
@@ -1030,7 +1186,8 @@ size_t step_scratch_bytes() {
 }
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
-  auto kern = fused ? step_kernel<true> : step_kernel<false>;
+  const bool mx = fused && a.y_scale != nullptr;
+  auto kern = mx ? step_kernel<true, true> : fused ? step_kernel<true> : step_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int ctas = 0;
@@ -1042,16 +1199,20 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   const int tt = shape.tt;
   const int ngroups = std::max(1, shape.groups);
   const int tiles = static_cast<int>((a.N + tt - 1) / tt);
-  CUtensorMap tx, tf, txo, ty;
+  CUtensorMap tx, tf, txo, ty, ty8;
   if (!map_streams(&tx, a.X, a.N, a.d, tt)) return cudaErrorInvalidValue;
   if (fused) {
     if (!map_rows(&tf, a.F, a.N, a.d, tt)) return cudaErrorInvalidValue;
     if (!map_streams(&txo, a.X_out, a.N, a.d, tt)) return cudaErrorInvalidValue;
-    if (!map_rows(&ty, a.y_out, a.N, a.d, tt)) return cudaErrorInvalidValue;
+    if (!(mx ? map_codes(&ty, a.y_out, a.N, a.d, std::min(tt, 32)) : map_rows(&ty, a.y_out, a.N, a.d, tt)))
+      return cudaErrorInvalidValue;
+    if (mx ? !map_codes(&ty8, a.y_out, a.N, a.d, 8) : false) return cudaErrorInvalidValue;
+    if (!mx) ty8 = ty;
   } else {
     tf = tx;
     txo = tx;
     ty = tx;
+    ty8 = tx;
   }
 
   StepParams P{};
@@ -1066,6 +1227,7 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   P.post_out = a.post_out;
   P.comb_out = a.comb_out;
   P.mixes_out = a.mixes_out;
+  P.y_scale = mx ? a.y_scale : nullptr;
   P.status = status_word();
   if (P.status == nullptr) return cudaErrorInvalidDevice;
   P.trace = trace_buffer(static_cast<int64_t>(split) * tiles);
@@ -1099,7 +1261,7 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tx, tf, txo, ty, P);
+  return cudaLaunchKernelEx(&cfg, kern, tx, tf, txo, ty, ty8, P);
 }
 
 cudaError_t step_resident_ctas(int* ctas) {

@@ -25,7 +25,8 @@ struct StepArgs {
   const float* base;
   const float* gain;        // fused step only
   void* X_out;              // fused step only
-  void* y_out;              // fused step only
+  void* y_out;              // fused step only: bf16 [N, d], or E4M3 codes [N, d] with y_scale
+  uint8_t* y_scale;         // MXFP8 y only: E8M0 scale codes [N, d / 32]; null for bf16 y
   float* pre_out;
   float* post_out;
   float* comb_out;

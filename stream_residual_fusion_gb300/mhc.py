@@ -56,6 +56,7 @@ SIGNATURES = {
     "mhc_packed_block_columns": (_I, []),
     "mhc_fused_step": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_fused_step_packed": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
+    "mhc_fused_step_mxfp8": (_I, [_P] * 16 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_step_scratch_bytes": (_SZ, [_I, _I]),
     "mhc_fused_step_noalloc": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P]),
     "mhc_noalloc_scratch_bytes": (_SZ, []),
@@ -163,15 +164,16 @@ def _step_outputs(X, out, with_mixes):
     pin = dev.type == "cpu"                    # host outputs of fused_step_host: page-locked
     out = dict(out or {})
 
-    def new(shape, dtype):
-        return torch.empty(shape, dtype=dtype, device=dev, pin_memory=pin)
-    out.setdefault("Xp", new(X.shape, torch.bfloat16))
-    out.setdefault("y", new((N, d), torch.bfloat16))
-    out.setdefault("pre", new((N, n), torch.float32))
-    out.setdefault("post", new((N, n), torch.float32))
-    out.setdefault("comb", new((N, n, n), torch.float32))
+    def need(key, shape, dtype):               # allocate only what the caller did not pass
+        if key not in out:
+            out[key] = torch.empty(shape, dtype=dtype, device=dev, pin_memory=pin)
+    need("Xp", X.shape, torch.bfloat16)
+    need("y", (N, d), torch.bfloat16)
+    need("pre", (N, n), torch.float32)
+    need("post", (N, n), torch.float32)
+    need("comb", (N, n, n), torch.float32)
     if with_mixes:
-        out.setdefault("mixes", new((N, MIX), torch.float32))
+        need("mixes", (N, MIX), torch.float32)
     return out
 
 
@@ -208,6 +210,41 @@ def fused_step(X, F, pre_prev, post_prev, comb_prev, W, scale, base, gain, *, it
             _ptr(scale), _ptr(base), _ptr(gain), *common_out, N, n, d, iters, hc_eps, norm_eps,
             flags, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
         _check(rc, "mhc_fused_step")
+    return o
+
+
+MX_BLOCK = 32   # features per MXFP8 block (one E8M0 scale each)
+
+
+def fused_step_mxfp8(X, F, pre_prev, post_prev, comb_prev, W_packed, scale, base, gain, *,
+                     iters=20, hc_eps=1e-6, norm_eps=1e-6, flags=0, with_mixes=False, out=None,
+                     scratch=None, stream=None):
+    """mhc_fused_step_mxfp8: the fused step with y written as MXFP8 (E4M3 codes `y_codes`
+    uint8 [N, d] and E8M0 block scales `y_scale` uint8 [N, d/32]) instead of bf16 y. Returns
+    dict with Xp, y_codes, y_scale, pre, post, comb (and mixes)."""
+    _need(X, torch.bfloat16, "X")
+    _need(F, torch.bfloat16, "F")
+    _need(W_packed, torch.uint8, "W_packed")
+    for t, nm in ((pre_prev, "pre_prev"), (post_prev, "post_prev"), (comb_prev, "comb_prev"),
+                  (scale, "scale"), (base, "base"), (gain, "gain")):
+        _need(t, torch.float32, nm)
+    N, n, d = X.shape
+    o = dict(out or {})
+    if "y_codes" not in o:
+        o["y_codes"] = torch.empty(N, d, dtype=torch.uint8, device=X.device)
+    if "y_scale" not in o:
+        o["y_scale"] = torch.empty(N, d // MX_BLOCK, dtype=torch.uint8, device=X.device)
+    o["y"] = o["y_codes"]                        # _step_outputs fills the rest, not y
+    o = _step_outputs(X, o, with_mixes)
+    del o["y"]
+    if scratch is None:
+        scratch = torch.empty(step_scratch_bytes(d, n), dtype=torch.uint8, device=X.device)
+    rc = lib.mhc_fused_step_mxfp8(
+        _ptr(X), _ptr(F), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev), _ptr(W_packed),
+        _ptr(scale), _ptr(base), _ptr(gain), _ptr(o["Xp"]), _ptr(o["y_codes"]), _ptr(o["y_scale"]),
+        _ptr(o["pre"]), _ptr(o["post"]), _ptr(o["comb"]), _ptr(o.get("mixes")), N, n, d, iters,
+        hc_eps, norm_eps, flags, _ptr(scratch), scratch.numel(), _stream(stream))
+    _check(rc, "mhc_fused_step_mxfp8")
     return o
 
 
@@ -289,11 +326,12 @@ def mixes(X, W, scale, base, *, iters=20, hc_eps=1e-6, norm_eps=1e-6, flags=0, w
     N, n, d = X.shape
     dev = X.device
     o = dict(out or {})
-    o.setdefault("pre", torch.empty(N, n, dtype=torch.float32, device=dev))
-    o.setdefault("post", torch.empty(N, n, dtype=torch.float32, device=dev))
-    o.setdefault("comb", torch.empty(N, n, n, dtype=torch.float32, device=dev))
+    shapes = {"pre": (N, n), "post": (N, n), "comb": (N, n, n)}
     if with_mixes:
-        o.setdefault("mixes", torch.empty(N, MIX, dtype=torch.float32, device=dev))
+        shapes["mixes"] = (N, MIX)
+    for key, shape in shapes.items():        # allocate only what the caller did not pass
+        if key not in o:
+            o[key] = torch.empty(shape, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = torch.empty(workspace_bytes(d, n), dtype=torch.uint8, device=dev)
     rc = lib.mhc_mixes(_ptr(X), _ptr(W), _ptr(scale), _ptr(base), _ptr(o.get("mixes")),

@@ -6,6 +6,11 @@ Tolerances (stated once, used by every GPU test):
   * y: within 2 bf16 ulps of the oracle (the RMS statistic is summed in a different order).
   * p, u, C: absolute error <= 1e-5.
   * m (the 24 mix numbers): per token, max |dm| <= 1e-4 * max |m|.
+  * MXFP8 y: the codes encode the kernel's bf16 y, which is within Y_ULPS bf16 ulps of the
+    oracle's. Scales and codes must equal the oracle's encoding of its y wherever no y within
+    that distance would decide otherwise (a block maximum that close to a power of two, y / X
+    that close to a boundary between E4M3 values); there the kernel's result must be one of the
+    two decisions within reach.
 """
 import numpy as np
 
@@ -73,3 +78,32 @@ def check_step(out, ref, with_mixes=True):
         assert_abs(to64(out[k]), ref[k], TOL_PUC, k)
     if with_mixes:
         assert_mixes(to64(out["mixes"]), ref["mixes"])
+
+
+def check_mxfp8(codes, scale, y_ref, ulps=Y_ULPS):
+    """codes uint8 [N, d], scale uint8 [N, d/32] from the kernel against the oracle's MXFP8
+    encoding (oracle.mx) of its bf16 y [N, d]."""
+    from oracle import mx
+    codes = np.asarray(codes)
+    scale = np.asarray(scale).astype(np.int64)
+    N, d = y_ref.shape
+    wid = ulps * bf16_ulp(y_ref)
+    a_lo = np.maximum(np.abs(y_ref) - wid, 0.0).reshape(N, d // mx.MX_BLOCK, mx.MX_BLOCK).max(axis=2)
+    a_hi = (np.abs(y_ref) + wid).reshape(N, d // mx.MX_BLOCK, mx.MX_BLOCK).max(axis=2)
+    s_lo = mx.mx_scale_code(a_lo).astype(np.int64)
+    s_hi = mx.mx_scale_code(a_hi).astype(np.int64)
+    ok_s = (scale >= s_lo) & (scale <= s_hi)
+    if not ok_s.all():
+        i = np.argwhere(~ok_s)[0]
+        raise AssertionError(f"y_scale: {int((~ok_s).sum())} of {ok_s.size} blocks differ; first "
+                             f"at {i.tolist()}: got {scale[tuple(i)]}, want {s_lo[tuple(i)]}")
+    X = np.repeat(np.exp2(scale.astype(np.float64) - 127.0), mx.MX_BLOCK, axis=1)
+    got = mx.e4m3_decode(codes)
+    lo, hi = mx.e4m3_round((y_ref - wid) / X), mx.e4m3_round((y_ref + wid) / X)
+    ok = (got >= lo) & (got <= hi)
+    if not ok.all():
+        i = np.argwhere(~ok)[0]
+        raise AssertionError(f"y codes: {int((~ok).sum())} of {ok.size} differ; first at "
+                             f"{i.tolist()}: got {got[tuple(i)]}, want {mx.e4m3_round(y_ref[tuple(i)] / X[tuple(i)])}")
+    same = (scale == mx.mx_scale_code(np.abs(y_ref).reshape(N, -1, mx.MX_BLOCK).max(axis=2))).mean()
+    assert same > 0.99, f"y_scale: only {same:.4f} of the blocks equal the oracle's"
