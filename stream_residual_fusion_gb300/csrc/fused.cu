@@ -116,10 +116,18 @@ __host__ __device__ constexpr int ftile(int b) { return b * STAGE_BYTES + 4 * TI
 __host__ __device__ constexpr int wtile(int e, int k) {
   return OFF_W + e * STEP_WBLOCK_BYTES + k * STEP_WSTREAM_BYTES;
 }
-// y staging at the very end reuses the X/F tiles of the idle ring: slot j -> stage j/5, tile j%5.
-__host__ __device__ constexpr int yslot(int j) { return (j / 5) * STAGE_BYTES + (j % 5) * TILE_BYTES; }
-constexpr int NYSLOTS = 5 * NSTAGE;
-constexpr int EB = 4;                   // stash slots the epilogue loads per TMEM wait
+// y staging at the very end reuses the X/F tiles of the idle ring (slot j -> stage j/5, tile
+// j%5) and, from j = 5 NSTAGE on, the idle weight ring, so the last R <= NYSLOTS slots of y are
+// staged at once.
+__host__ __device__ constexpr int yslot(int j) {
+  return j < 5 * NSTAGE ? (j / 5) * STAGE_BYTES + (j % 5) * TILE_BYTES : OFF_W + (j - 5 * NSTAGE) * TILE_BYTES;
+}
+constexpr int NYSLOTS = 5 * NSTAGE + NW * STEP_WBLOCK_BYTES / TILE_BYTES;
+static_assert(NW * STEP_WBLOCK_BYTES % TILE_BYTES == 0, "weight ring holds whole staging tiles");
+static_assert(STASH_SLOTS <= NYSLOTS, "the stash's slots of y are staged in one batch");
+constexpr int EB = 4;                   // stash slots the MXFP8 epilogue loads per TMEM wait
+constexpr int GAIN_PER_THREAD = (MAX_SLICE + NCONS * 32 - 1) / (NCONS * 32);   // epilogue gains
+static_assert(STASH_SLOTS < NYSLOTS, "the gains' staging tile is not a y staging tile");
 
 struct StepParams {
   const float* pre_prev;
@@ -179,16 +187,19 @@ __device__ __forceinline__ void fold_group(uint32_t tmem_lane, int gg, int h, fl
   }
 }
 
-// y = bf16(gain * (y_hat * r)) for the 8 columns starting at `col`.
-__device__ __forceinline__ uint4 rms_scale8(const uint32_t* w, const float* __restrict__ gain,
-                                            int col, f2 r2) {
-  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain + col));
-  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain + col + 4));
+// y = bf16(gain * (y_hat * r)) for 8 columns whose gains are g0, g1.
+__device__ __forceinline__ uint4 rms_scale8(const uint32_t* w, float4 g0, float4 g1, f2 r2) {
   const f2 gp[4] = {f2{g0.x, g0.y}, f2{g0.z, g0.w}, f2{g1.x, g1.y}, f2{g1.z, g1.w}};
   uint32_t o[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) o[e] = f2_to_bf2(mul2(gp[e], mul2(bf2_to_f2(w[e]), r2)));
   return make_uint4(o[0], o[1], o[2], o[3]);
+}
+// ... for the 8 columns starting at `col`.
+__device__ __forceinline__ uint4 rms_scale8(const uint32_t* w, const float* __restrict__ gain,
+                                            int col, f2 r2) {
+  return rms_scale8(w, __ldg(reinterpret_cast<const float4*>(gain + col)),
+                    __ldg(reinterpret_cast<const float4*>(gain + col + 4)), r2);
 }
 
 // MXFP8 y (OCP Microscaling formats v1.0: E4M3 elements, blocks of 32 features of a token that
@@ -196,11 +207,10 @@ __device__ __forceinline__ uint4 rms_scale8(const uint32_t* w, const float* __re
 // MXFP8 pass over the y that the bf16 path writes. A slot row is one block; each of the token's
 // two consumer threads holds 16 of its features.
 // This thread's 16 bf16 y values, packed in pairs: those of the bf16 path.
-__device__ __forceinline__ void y_bf16x16(const uint32_t* w, const float* __restrict__ gain,
-                                          int col, f2 r2, uint32_t* y) {
+__device__ __forceinline__ void y_bf16x16(const uint32_t* w, const float4* g, f2 r2, uint32_t* y) {
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    const uint4 v = rms_scale8(w + 4 * q, gain, col + 8 * q, r2);
+    const uint4 v = rms_scale8(w + 4 * q, g[2 * q], g[2 * q + 1], r2);
     y[4 * q] = v.x;
     y[4 * q + 1] = v.y;
     y[4 * q + 2] = v.z;
@@ -732,7 +742,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               // TMEM quarter); after their barrier both have also read their F rows, which then
               // take the quarter's codes (code_offset)
               uint32_t yv[8];
-              y_bf16x16(prev, P.gain, ycol + chunk0 * 8, r_src, yv);
+              float4 gv[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                gv[i] = __ldg(reinterpret_cast<const float4*>(P.gain + ycol + chunk0 * 8) + i);
+              y_bf16x16(prev, gv, r_src, yv);
               const uint32_t e_own = amax_exponent16(yv);
               uint8_t* xch = sm + OFF_XCH + (gs & 1) * (2 * TT);
               xch[part * TT + tl] = static_cast<uint8_t>(e_own);
@@ -805,31 +819,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (FUSED && it > 0) {
       // y still in the stash: the last R global slots (tile it-1's slots and, before them, the
       // last RLAG slots of tile it-2)
+      // The gains of the CTA's S column blocks go to the last staging tile, in the idle weight
+      // ring (this thread has folded the last group, so every MMA is done); their loads are in
+      // flight during the RMS-factor wait.
+      float* gsm = reinterpret_cast<float*>(sm + yslot(NYSLOTS - 1));
+      const int ct = static_cast<int>(threadIdx.x) - NROLE * 32;
+      float gl[GAIN_PER_THREAD];
+#pragma unroll
+      for (int k = 0; k < GAIN_PER_THREAD; ++k) {
+        const int i = ct + k * NCONS * 32;
+        gl[k] = i < S * DC ? __ldg(P.gain + col0 + (i / DC) * cstride + i % DC) : 0.f;
+      }
       rms_issue(it - 1);
       const f2 r_last = rms_finish();
       const f2 r_before = r_new;    // tile it-2's factor (computed during tile it-1)
+#pragma unroll
+      for (int k = 0; k < GAIN_PER_THREAD; ++k) {
+        const int i = ct + k * NCONS * 32;
+        if (i < S * DC) gsm[i] = gl[k];
+      }
       if (!mbar_wait(drained, 0, limit())) timed_out = true;   // the ring is idle now
+      named_bar_sync(1, NCONS * 32);                            // and the gains are in place
       const uint64_t stream_pol = policy_evict_first();
       const int first = std::max(0, gs - R);
+      const int boundary = (it - 1) * S;    // slots below it are tile it-2's
+      int ring = first % R, sidx = first % S;
       for (int g0 = first; g0 < gs; g0 += NYSLOTS) {
         const int g1 = std::min(gs, g0 + NYSLOTS);
         if constexpr (MX) {
-          // EB stash slots per TMEM wait (the bf16 loop below measured faster one at a time).
-          // As in the main loop, the block maxima go through the spare kilobyte of each staged
-          // slot's quarter: one pair barrier per EB slots.
+          // EB stash slots per TMEM wait. As in the main loop, the block maxima go through the
+          // spare kilobyte of each staged slot's quarter: one pair barrier per EB slots.
           for (int b0 = g0; b0 < g1; b0 += EB) {
-            uint32_t w[EB][PASS_COLS];
+            uint32_t w[EB][PASS_COLS], yv[EB][8], e_own[EB], col[EB];
 #pragma unroll
-            for (int e = 0; e < EB; ++e)
-              if (b0 + e < g1) stash_load_nowait(slot_addr((b0 + e) % R), w[e]);
+            for (int e = 0; e < EB; ++e) {
+              col[e] = 0;
+              if (b0 + e < g1) {
+                stash_load_nowait(slot_addr(ring), w[e]);
+                col[e] = sidx;
+                ring = ring + 1 == R ? 0 : ring + 1;
+                sidx = sidx + 1 == S ? 0 : sidx + 1;
+              }
+            }
             tmem_ld_wait();
-            uint32_t yv[EB][8], e_own[EB];
 #pragma unroll
             for (int e = 0; e < EB; ++e) {
               const int src = b0 + e;
               if (src < g1) {
-                const f2 r = (src / S == it - 1) ? r_last : r_before;
-                y_bf16x16(w[e], P.gain, col0 + (src % S) * cstride + chunk0 * 8, r, yv[e]);
+                y_bf16x16(w[e], reinterpret_cast<const float4*>(gsm + col[e] * DC + chunk0 * 8),
+                          src >= boundary ? r_last : r_before, yv[e]);
                 e_own[e] = amax_exponent16(yv[e]);
                 sm[yslot(src - g0) + sub * 2048 + 1024 + part * 32 + lane] = static_cast<uint8_t>(e_own[e]);
               }
@@ -844,21 +882,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 *reinterpret_cast<uint4*>(sm + yslot(src - g0) + code_offset(tl, part)) = mx_encode16(yv[e], code);
                 const int token = (c0 + (src / S) * nclust) * tt + tl;
                 if (part == 0 && tl < tt && token < P.N)
-                  P.y_scale[static_cast<size_t>(token) * (P.d / 32) + (col0 + (src % S) * cstride) / 32] =
+                  P.y_scale[static_cast<size_t>(token) * (P.d / 32) + (col0 + col[e] * cstride) / 32] =
                       static_cast<uint8_t>(code);
               }
             }
           }
         } else {
           for (int src = g0; src < g1; ++src) {
-            const f2 r = (src / S == it - 1) ? r_last : r_before;
             uint32_t w[PASS_COLS];
-            stash_load(slot_addr(src % R), w);
-            const int col = col0 + (src % S) * cstride;
+            stash_load(slot_addr(ring), w);
+            const float4* gp = reinterpret_cast<const float4*>(gsm + sidx * DC + chunk0 * 8);
+            const f2 r = src >= boundary ? r_last : r_before;
 #pragma unroll
             for (int q = 0; q < CPH; ++q)
               *reinterpret_cast<uint4*>(sm + yslot(src - g0) + row_off[q]) =
-                  rms_scale8(w + 4 * q, P.gain, col + (chunk0 + q) * 8, r);
+                  rms_scale8(w + 4 * q, gp[2 * q], gp[2 * q + 1], r);
+            ring = ring + 1 == R ? 0 : ring + 1;
+            sidx = sidx + 1 == S ? 0 : sidx + 1;
           }
         }
         fence_proxy_async_smem();
