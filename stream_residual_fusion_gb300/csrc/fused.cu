@@ -950,21 +950,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // reuse their partials buffers
         for (int base_t = 0; base_t < per; base_t += 16) {
           float4 s0[2], s1[2], s2[2], s6[2];
+          int tl2[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             s0[u] = s1[u] = s2[u] = s6[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int tl2 = static_cast<int>(g) * per + min(base_t + 8 * u + q, per - 1);
-            for (int rk = 0; rk < split; ++rk) {
-              const float4* row = reinterpret_cast<const float4*>(gpart(pb, rk) + tl2 * PART_STRIDE);
-              const float4 v0 = __ldcg(row);
-              const float4 v1 = __ldcg(row + 1);
-              const float4 v2 = __ldcg(row + 2 + j);
-              const float4 v6 = __ldcg(row + 6);
-              s0[u].x += v0.x; s0[u].y += v0.y; s0[u].z += v0.z; s0[u].w += v0.w;
-              s1[u].x += v1.x; s1[u].y += v1.y; s1[u].z += v1.z; s1[u].w += v1.w;
-              s2[u].x += v2.x; s2[u].y += v2.y; s2[u].z += v2.z; s2[u].w += v2.w;
-              s6[u].x += TPT == 4 ? (v6.x + v6.y) + (v6.z + v6.w) : v6.x + v6.y;   // S_x parts
-            }
+            tl2[u] = static_cast<int>(g) * per + min(base_t + 8 * u + q, per - 1);
+          }
+          // two ranks' rows of both tokens in flight per round trip; added in rank order
+          for (int rk = 0; rk < split; rk += 2) {
+            float4 v[2][2][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+              for (int o = 0; o < 2; ++o) {
+                const float4* row = reinterpret_cast<const float4*>(
+                    gpart(pb, min(rk + o, split - 1)) + tl2[u] * PART_STRIDE);
+                v[u][o][0] = __ldcg(row);
+                v[u][o][1] = __ldcg(row + 1);
+                v[u][o][2] = __ldcg(row + 2 + j);
+                v[u][o][3] = __ldcg(row + 6);
+              }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+              for (int o = 0; o < 2; ++o) {
+                if (rk + o >= split) continue;
+                const float4 v0 = v[u][o][0], v1 = v[u][o][1], v2 = v[u][o][2], v6 = v[u][o][3];
+                s0[u].x += v0.x; s0[u].y += v0.y; s0[u].z += v0.z; s0[u].w += v0.w;
+                s1[u].x += v1.x; s1[u].y += v1.y; s1[u].z += v1.z; s1[u].w += v1.w;
+                s2[u].x += v2.x; s2[u].y += v2.y; s2[u].z += v2.z; s2[u].w += v2.w;
+                s6[u].x += TPT == 4 ? (v6.x + v6.y) + (v6.z + v6.w) : v6.x + v6.y;   // S_x parts
+              }
           }
           if (base_t + 16 >= per) {
             // every read of buffer pb is done: the group may reuse it
