@@ -109,6 +109,36 @@ def test_fused_validation(M):
     assert _fused(M, N=0) == M.MHC_OK                    # nothing to do, nothing launched
 
 
+def _mx(M, N=256, d=5120, ptrs=None):
+    p = [_addr(i) for i in range(16)] if ptrs is None else ptrs
+    return M.lib.mhc_fused_step_mxfp8(*p, N, 4, d, 20, 1e-6, 1e-6, 0, _addr(21), 1 << 26, None)
+
+
+def test_mxfp8_validation(M):
+    """The MXFP8-y entry: its scale pointer is required and aligned, and the codes take one byte
+    per element when overlaps are checked (host-side checks, before any device call)."""
+    assert _mx(M, N=0) == M.MHC_OK
+    p = [_addr(i) for i in range(16)]
+    p[11] = None                                         # y_scale
+    assert _mx(M, ptrs=p) == M.MHC_ERR_NULL
+    p = [_addr(i) for i in range(16)]
+    p[11] = ctypes.c_void_p(p[11].value + 4)
+    assert _mx(M, ptrs=p) == M.MHC_ERR_ALIGN
+    N, d = 256, 5120
+    p = [_addr(i) for i in range(16)]
+    p[11] = ctypes.c_void_p(p[10].value + N * d - 16)     # scales inside the codes
+    assert _mx(M, ptrs=p) == M.MHC_ERR_ALIAS
+    p = [_addr(i) for i in range(16)]
+    p[11] = ctypes.c_void_p(p[10].value + N * d)          # right after them: no overlap
+    assert _mx(M, ptrs=p) != M.MHC_ERR_ALIAS
+    p = [_addr(i) for i in range(16)]
+    p[12] = ctypes.c_void_p(p[11].value + N * d // 32 - 16)   # pre_out inside the scales
+    assert _mx(M, ptrs=p) == M.MHC_ERR_ALIAS
+    p = [_addr(i) for i in range(16)]
+    p[10] = ctypes.c_void_p(p[1].value - N * d)           # codes end where F begins
+    assert _mx(M, ptrs=p) != M.MHC_ERR_ALIAS
+
+
 def test_split_choices(M):
     B = M.lib.mhc_packed_block_columns()
     # d/split a multiple of 32 (whole pipeline slots) in [128, 640] for some split <= 32
