@@ -931,6 +931,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     //     r + L, ... (two ranks' loads in flight at a time), a shuffle butterfly combines the L
     //     sums (the same total in every lane), and every lane runs the whole Sinkhorn
     //     (split_sinkhorn_all, no shuffle latency); lanes r < 4 write row r.
+    // the split parameters, read by every token's split: into L1 before the first tile
+    if (lane < 24) prefetch_l1(P.base + lane);
+    if (lane == 24) prefetch_l1(P.scale);
     const int q = lane >> 2;
     const int j = lane & 3;
     const int per = tt / split;
@@ -981,11 +984,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 s2[u].x += v2.x; s2[u].y += v2.y; s2[u].z += v2.z; s2[u].w += v2.w;
                 s6[u].x += TPT == 4 ? (v6.x + v6.y) + (v6.z + v6.w) : v6.x + v6.y;   // S_x parts
               }
-          }
-          if (base_t + 16 >= per) {
-            // every read of buffer pb is done: the group may reuse it
-            __syncwarp();
-            if (lane == 0) gcount_release(&pfree[pb]);
           }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -1044,11 +1042,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int off = 1; off < L; off <<= 1)
 #pragma unroll
             for (int e = 0; e < NACC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-          if (base_t + TP >= per) {
-            // every read of buffer pb is done: the group may reuse it
-            __syncwarp();
-            if (lane == 0) gcount_release(&pfree[pb]);
-          }
           const int token2 = t0 + static_cast<int>(g) * per + tt_;
           float sxt = 0.f;
 #pragma unroll
@@ -1083,6 +1076,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
           }
         }
+      }
+      // every read of exchange buffer pb is done: the group may reuse it for tile it + 2 (if
+      // any). Released after the tile's outputs, off the path to them: the release waits for
+      // this lane's earlier memory operations.
+      if (tile + 2 * nclust < ntiles) {
+        __syncwarp();
+        if (lane == 0) gcount_release(&pfree[pb]);
       }
       if (lane == 0) {
         if (auto tr = trace_rec(tile)) tr[5] = global_timer_ns();

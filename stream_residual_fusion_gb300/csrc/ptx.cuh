@@ -390,6 +390,10 @@ __device__ __forceinline__ unsigned gload_acquire(const unsigned* ctr) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
   return v;
 }
+// Prefetch the line holding p into L1.
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.L1 [%0];" ::"l"(p));
+}
 // Waits until *ctr >= target, polling every ~128 ns, giving up after limit_ns.
 __device__ __forceinline__ bool gwait(const unsigned* ctr, unsigned target, uint64_t limit_ns) {
   if (static_cast<int>(gload_acquire(ctr) - target) >= 0) return true;
