@@ -73,6 +73,28 @@ def test_mxfp8_parity(M, synth, N, d, split, tile):
     check_mxfp8(q["y_codes"].cpu().numpy(), q["y_scale"].cpu().numpy(), ref["y"])
 
 
+def test_mxfp8_comb_row_dest_in_place_no_mixes(M, synth):
+    """The other comb reading, X' written over X, and no m output: X', p, u, C equal the bf16
+    step's, the codes equal the cast of its y."""
+    N, d = 257, 5120
+    inp = synth.make_inputs(N, 4, d, seed=6200, device=DEV, scale_uniform=True)
+    inp["comb"] = torch.rand(N, 4, 4, device=DEV)      # not symmetric: the readings differ
+    Wp = M.pack_weights(inp["W"])
+    tail = (inp["scale"], inp["base"], inp["gain"])
+    bf = M.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None, *tail,
+                      W_packed=Wp, flags=M.COMB_ROW_DEST)
+    X = inp["X"].clone()
+    q = M.fused_step_mxfp8(X, inp["F"], inp["pre"], inp["post"], inp["comb"], Wp, *tail,
+                           flags=M.COMB_ROW_DEST, out={"Xp": X})
+    assert M.get_status() == M.MHC_OK
+    assert q["Xp"].data_ptr() == X.data_ptr() and "mixes" not in q
+    for k in ("Xp", "pre", "post", "comb"):
+        assert torch.equal(bf[k], q[k]), k
+    _same_as_cast(q, bf["y"])
+    ref = oracle_step(inp, comb_row_dest=True)
+    check_mxfp8(q["y_codes"].cpu().numpy(), q["y_scale"].cpu().numpy(), ref["y"])
+
+
 def test_mxfp8_zero_and_wide_range_tokens(M, synth):
     """A token whose streams and sublayer output are all zero gets scale code 0 and zero codes;
     tokens scaled by 2^-40 and 2^30 keep their codes and move their scales by -40 and +30."""
