@@ -253,13 +253,20 @@ def run_ours(args):
     scratch = torch.empty(mhc.step_scratch_bytes(d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # launch-shape flags (default: the library's automatic choice)
+    shape_flags = ((mhc.split_flag(args.split) if args.split else 0) |
+                   (mhc.tile_flag(args.tile) if args.tile else 0))
+    if args.prepacked:
+        mhc.pack_weights(inp["W"], out=Wp, stream=stream)
+
     def step(ev_a=None, ev_b=None):
-        mhc.pack_weights(inp["W"], out=Wp, stream=stream)                    # launch 1
+        if not args.prepacked:
+            mhc.pack_weights(inp["W"], out=Wp, stream=stream)                # launch 1
         if ev_a is not None:
             ev_a.record(stream)
         mhc.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None,
                        inp["scale"], inp["base"], inp["gain"], W_packed=Wp, scratch=scratch,
-                       out=out, stream=stream)                               # launch 2
+                       out=out, stream=stream, flags=shape_flags)            # launch 2
         if ev_b is not None:
             ev_b.record(stream)
 
@@ -368,20 +375,23 @@ def run_ours(args):
                    "sinkhorn_iters": 20, "comb_reading": "code: X'_k = u_k F + sum_j C_jk X_j",
                    "l2": (f"inputs larger than L2 ({N * 51200 / 1e9:.2f} GB of streams read per step)"
                           if N * 51200 > 129e6 else "inputs smaller than L2 (not flushed)"),
-                   "step": ("CUDA-graph replay of mhc_pack_weights + mhc_fused_step_packed"
-                            if args.graph else "mhc_pack_weights + mhc_fused_step_packed")},
+                   "step": (("CUDA-graph replay of " if args.graph else "") +
+                            ("mhc_fused_step_packed (weights packed once, before timing)"
+                             if args.prepacked else "mhc_pack_weights + mhc_fused_step_packed")),
+                   "launch_shape": dict(zip(("split", "tile", "groups"),
+                                            mhc.step_config(N, d, shape_flags)[:3]))},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / 8000.0,
                      "kernel": ("step_kernel<true> (fused), timed with the packing as one graph replay"
-                                if args.graph else "step_kernel<true> (fused)"),
+                                if args.graph and not args.prepacked else "step_kernel<true> (fused)"),
                      "kernel_ms_avg": fused_avg, "kernel_ms_p50": statistics.median(fused_ms),
                      "kernel_ms_p95": sorted(fused_ms)[int(0.95 * (len(fused_ms) - 1))],
                      "kernel_ms_p99": sorted(fused_ms)[int(0.99 * (len(fused_ms) - 1))],
                      "algorithmic_bytes_per_launch": algorithmic_bytes(N, d)},
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "gpu_launches": 2 * K,
+        "gpu_launches": (1 if args.prepacked else 2) * K,
         "status": "ok" if status == mhc.MHC_OK else "device wait gave up",
         "gpu": torch.cuda.get_device_name(dev),
         "torch": torch.__version__,
@@ -585,6 +595,13 @@ def main():
     ap.add_argument("--form", choices=("fused", "unfused", "mxfp8"), default="fused",
                     help="unfused: time the four-kernel form beside the fused step; mxfp8: the "
                          "step with MXFP8 y beside the bf16-y step (one GPU each)")
+    ap.add_argument("--prepacked", action="store_true",
+                    help="pack the weights once before timing (as a decode loop does); the step is "
+                         "then the fused launch alone")
+    ap.add_argument("--split", type=int, default=0,
+                    help="force the CTAs per tile (MHC_SPLIT flags); 0 = automatic")
+    ap.add_argument("--tile", type=int, default=0,
+                    help="force the tokens per tile (MHC_TILE flags); 0 = automatic")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="synthetic workload (default: the B=4,T=8192 prefill; others are for profiling)")
     args = ap.parse_args()
