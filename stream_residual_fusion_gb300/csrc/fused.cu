@@ -11,10 +11,12 @@
 //   * Each CTA owns d/split columns of every stream (d = 5120: 8 CTAs x 640 columns). The CTAs'
 //     columns interleave in slots of STEP_DC columns, so at every slot the group reads one
 //     contiguous run of STEP_DC*split columns of each token row.
-//   * Warp 0 drives the X/F ring: per slot, [128 tokens x STEP_DC] tiles of X_0..X_3 and F
-//     (tensor copies). The packed projection weights (32-column blocks, packed as the exact
+//   * Warp 0, lane 0 drives the X/F ring: per slot, [128 tokens x STEP_DC] tiles of X_0..X_3 and
+//     F (tensor copies). The packed projection weights (32-column blocks, packed as the exact
 //     shared-memory image the tensor cores read) flow through a ring of their own that the MMA
-//     thread refills, so weight traffic never holds up the stream loads.
+//     thread refills, so weight traffic never holds up the stream loads. Lane 1 (the poster)
+//     does the CTA's group-counter releases and polls and bulk-copies each tile's previous
+//     coefficients (p, u, C) into shared memory ahead of time.
 //   * 8 consumer warps (2 threads per token) compute hc_post in place in shared memory, its sum
 //     of squares, hc_pre and its sum of squares; y_hat goes to a TMEM stash. While doing so they
 //     normalise the previous tile's y_hat from the same stash slot into the F tile they just
@@ -25,8 +27,13 @@
 //   * Warp 10 stores X' and y with TMA straight from the slot's tiles and frees the slot as soon
 //     as the stores have read it.
 //   * After a tile's last slot the consumers post their slice's partial sums to the group
-//     through a scratch area in global memory (L2) and release-ordered counters; warp 11
-//     finishes the tile's mix numbers (scale, split, Sinkhorn) while the consumers move on.
+//     through a scratch area in global memory (L2); the poster publishes them with
+//     release-ordered counters. Warp 11 finishes the tile's mix numbers (scale, split,
+//     Sinkhorn) while the consumers move on.
+//   * After a CTA's last tile the consumers normalise the y still in the stash into the idle
+//     rings' tiles and store it in one batch.
+// step_kernel<true, true> is the same step writing y as MXFP8 (E4M3 codes and E8M0 block
+// scales) instead of bf16.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
