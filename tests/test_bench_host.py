@@ -1,0 +1,35 @@
+"""Host-side pieces of bench.py (no GPU): the algorithmic byte counts it reports, checked against
+the oracle's pinned traffic counts, and the lookup of the committed ncu traffic summary."""
+import bench
+import oracle as O
+
+
+def test_algorithmic_bytes_match_the_traffic_counts():
+    # the oracle counts bf16 elements per token (pinned by tests/golden/traffic.txt)
+    fused = 2 * O.traffic_per_token(O.fused_traffic_steps(4, 5120))
+    unfused = 2 * O.traffic_per_token(O.unfused_traffic_steps(4, 5120))
+    assert bench.STREAM_BYTES_PER_TOKEN == fused == 102400
+    # previous p, u, C in and new p, u, C out: 2 x (16 + 16 + 64) bytes
+    assert bench.SMALL_BYTES_PER_TOKEN == 192
+    assert bench.algorithmic_bytes(32768) == 32768 * 102592 + 640 * 5120 + 4 * 5120
+    # the unfused chain: twice the stream traffic, the same small vectors
+    assert sum(bench.UNFUSED_BYTES_PER_TOKEN.values()) == unfused + 192 == 204992
+    # MXFP8 y: y's 10,240 bf16 bytes become 5,120 code bytes and 160 scale bytes
+    assert bench.MXFP8_BYTES_PER_TOKEN == 102592 - 10240 + 5120 + 160 == 97632
+
+
+def test_ncu_traffic_lookup(tmp_path, monkeypatch):
+    """The bench takes DRAM bytes per token from the committed summary only when it names the
+    current kernel sources."""
+    current = bench.kernel_source_hash()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    summary = prof / "fused_step_prefill_ncu.md"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: current)
+    summary.write_text(f"kernel source hash: `{current}`\n\ndram bytes per token: 100000\n")
+    assert bench.ncu_traffic(10) == 1_000_000
+    summary.write_text("kernel source hash: `0123456789abcdef`\n\ndram bytes per token: 100000\n")
+    assert bench.ncu_traffic(10) is None
+    summary.unlink()
+    assert bench.ncu_traffic(10) is None
