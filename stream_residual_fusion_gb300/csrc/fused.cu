@@ -910,14 +910,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         fence_proxy_async_smem();
         named_bar_sync(1, NCONS * 32);
-        if (warp == NROLE && lane == 0) {
+        if constexpr (MX) {
+          // four or more stores per staged slot: every consumer warp issues those of every
+          // NCONS-th slot (measured 10% faster at 4,096 tokens than one issuing thread)
+          if (lane == 0) {
+            for (int src = g0 + (warp - NROLE); src < g1; src += NCONS)
+              store_codes(&tm_y, &tm_y8, sm + yslot(src - g0), col0 + (src % S) * cstride,
+                          (c0 + (src / S) * nclust) * tt, tt, stream_pol);
+            bulk_commit();
+            bulk_wait_read<0>();
+          }
+        } else if (warp == NROLE && lane == 0) {
           for (int src = g0; src < g1; ++src) {
             const int ytile = c0 + (src / S) * nclust;
-            if constexpr (MX)
-              store_codes(&tm_y, &tm_y8, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, tt,
-                          stream_pol);
-            else
-              tma_store_2d_hint(&tm_y, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, stream_pol);
+            tma_store_2d_hint(&tm_y, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, stream_pol);
           }
           bulk_commit();
           bulk_wait_read<0>();
