@@ -18,7 +18,7 @@ Every function is pinned by tests under tests/ (tests/test_oracle_*.py); nothing
 "parity unpinned".
 """
 from .mhc import (  # noqa: F401
-    bf16_round, fl32, fma32, hc_post, hc_pre, hc_mixes_scores, hc_split, sinkhorn, sinkhorn_plain,
+    bf16_round, fl32, hc_post, hc_pre, hc_mixes_scores, hc_split, sinkhorn, sinkhorn_plain,
     hc_mixes, rmsnorm, fused_step, parameter_counts, traffic_per_token, unfused_traffic_steps,
     fused_traffic_steps, inputs_to_f64,
 )

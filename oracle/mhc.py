@@ -4,14 +4,13 @@ Precision. The pages' code runs every step in float32 torch ops on bf16 streams.
 computes the continuous results (the mix projection and its RMS scale, the split, Sinkhorn, the
 RMSNorm) in float64: they are compared against the GPU with tolerances. Two steps end in a bf16
 rounding whose result feeds later steps -- hc_post's X' (fed to the projection and to hc_pre) and
-hc_pre's y_hat (fed to the RMSNorm). There both sides must take the rounding decision in the same
-precision. The pages fix float32 for these steps (Stream weights for the feed-forward, Code:
-hc_pre and hc_post: float32 products summed over the stream index, then a cast to the stream
-dtype) but fix neither the order of the 4-term sum nor whether a product is rounded before it is
-added. The reading taken is the kernel's: each product is fused into the addition that consumes
-it (a float32 fused multiply-add, one rounding), the stream terms are summed left to right
-(j = 0, 1, 2, 3) and hc_post's sublayer term is added last. The oracle evaluates exactly those
-float32 operations (fma32 below is a correctly rounded float32 fused multiply-add).
+hc_pre's y_hat (fed to the RMSNorm). There the oracle evaluates the float32 arithmetic the pages'
+code spells out (Stream weights for the feed-forward, Code: hc_pre and hc_post): every product of
+a float32 weight and a stream element is its own float32 tensor, so each product is rounded to
+float32; the products are then summed over the stream index in float32, in index order
+(j = 0, 1, 2, 3, each addition rounded); hc_post adds its rounded sublayer product u_k * F to that
+sum; the float32 result is cast to bf16. numpy's float32 multiply and add are single IEEE
+operations (no fused multiply-add), so the code below is that evaluation as written.
 
 All arrays are numpy; bf16 values are carried as float64 holding exactly representable values.
 """
@@ -26,31 +25,6 @@ import numpy as np
 def fl32(x) -> np.ndarray:
     """Round to the nearest float32 (numpy's cast is IEEE round-to-nearest-even)."""
     return np.asarray(x, dtype=np.float64).astype(np.float32)
-
-
-def fma32(a, b, c) -> np.ndarray:
-    """float32 fused multiply-add: a*b + c rounded once to the nearest float32 (ties to even).
-
-    a, b, c are float32 (broadcastable). The product of two float32 numbers is exact in float64,
-    and the float64 sum s together with its TwoSum error e gives a*b + c = s + e exactly. Casting
-    s to float32 is then the correctly rounded result, except when s lies exactly halfway between
-    two float32 numbers while e != 0: the exact value is then off the tie, on the side of e.
-    """
-    p = np.asarray(a, np.float32).astype(np.float64) * np.asarray(b, np.float32).astype(np.float64)
-    c = np.asarray(c, np.float32).astype(np.float64)
-    p, c = np.broadcast_arrays(p, c)
-    s = p + c
-    bb = s - p
-    e = (p - (s - bb)) + (c - bb)                 # exact error of the float64 addition
-    r = s.astype(np.float32)
-    r64 = r.astype(np.float64)
-    up = np.nextafter(r, np.float32(np.inf)).astype(np.float64)
-    dn = np.nextafter(r, np.float32(-np.inf)).astype(np.float64)
-    below = r64 < s                               # s lies between r and up
-    above = r64 > s                               # s lies between dn and r
-    tie = np.where(below, 2 * (s - r64) == up - r64, np.where(above, 2 * (r64 - s) == r64 - dn, False))
-    out = np.where(tie & below & (e > 0), up, np.where(tie & above & (e < 0), dn, r64))
-    return out.astype(np.float32)
 
 
 _BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
@@ -93,12 +67,13 @@ def inputs_to_f64(inputs: dict) -> dict:
 def hc_post(X, F, post, comb, comb_row_dest: bool = False) -> np.ndarray:
     """Expand the sublayer output back to the streams and mix the residual in through comb.
 
-    Stream weights for the feed-forward, Code: hc_post. The excerpt forms
-    post[k]*x + sum over dim 2 of comb[j,k]*residual[j], i.e. X'_k = u_k F + sum_j C_jk X_j (the
-    sum runs over comb's first stream index), in float32, then casts to the stream dtype. Float32
-    order (module docstring): fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0)))).
-    `comb_row_dest=True` takes the other reading, X'_j = u_j F + sum_k C_jk X_k (element (i,j) of
-    comb as "from stream j into stream i", section 3 of "2A · Single-Pass mHC").
+    Stream weights for the feed-forward, Code: hc_post. The excerpt forms post[k]*x plus the sum
+    over comb's first stream index of comb[j,k]*residual[j], i.e.
+    X'_k = u_k F + sum_j C_jk X_j, in float32, then casts to the stream dtype. Float32 order
+    (module docstring): P_j = fl(C_jk X_j); S = ((P_0 + P_1) + P_2) + P_3; X'_k = fl(u_k F) + S,
+    each operation rounded to float32. `comb_row_dest=True` takes the other reading,
+    X'_j = u_j F + sum_k C_jk X_k (element (i,j) of comb as "from stream j into stream i",
+    section 3 of "2A · Single-Pass mHC").
 
     X [N,n,d], F [N,d], post [N,n], comb [N,n,n] -> X' [N,n,d] (bf16 values).
     """
@@ -111,10 +86,12 @@ def hc_post(X, F, post, comb, comb_row_dest: bool = False) -> np.ndarray:
     N, n, d = X.shape
     out = np.empty((N, n, d), dtype=np.float64)
     for k in range(n):
-        mixed = comb[:, 0, k, None] * X[:, 0, :]               # float32 product
-        for j in range(1, n):                                  # left to right, fused
-            mixed = fma32(comb[:, j, k, None], X[:, j, :], mixed)
-        out[:, k, :] = bf16_round(fma32(post[:, k, None], F, mixed).astype(np.float64))
+        mixed = comb[:, 0, k, None] * X[:, 0, :]               # float32 product, rounded
+        for j in range(1, n):                                  # sum over j in index order
+            mixed = mixed + comb[:, j, k, None] * X[:, j, :]   # rounded product, rounded sum
+        Xk = post[:, k, None] * F + mixed                      # rounded product, rounded sum
+        assert Xk.dtype == np.float32
+        out[:, k, :] = bf16_round(Xk.astype(np.float64))
     return out
 
 
@@ -123,7 +100,7 @@ def hc_pre(Xp, pre) -> np.ndarray:
 
     Stream weights for the feed-forward, Code: hc_pre (float32 products, sum over the stream
     index, cast to the stream dtype). Float32 order (module docstring):
-    fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0))).
+    Q_j = fl(p_j X'_j); y_hat = bf16(((Q_0 + Q_1) + Q_2) + Q_3), each operation rounded.
     X' [N,n,d], pre [N,n] -> y_hat [N,d] (bf16 values).
     """
     Xp = fl32(Xp)
@@ -131,7 +108,8 @@ def hc_pre(Xp, pre) -> np.ndarray:
     n = Xp.shape[1]
     acc = pre[:, 0, None] * Xp[:, 0, :]
     for j in range(1, n):
-        acc = fma32(pre[:, j, None], Xp[:, j, :], acc)
+        acc = acc + pre[:, j, None] * Xp[:, j, :]
+    assert acc.dtype == np.float32
     return bf16_round(acc.astype(np.float64))
 
 

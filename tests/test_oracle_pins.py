@@ -70,36 +70,135 @@ def _round_f32_exact(fr):
     return np.float32(best[0])
 
 
-def test_fma32_against_exact_rationals():
-    """Random float32 triples over a range of exponent gaps, and near-tie triples whose product
-    has few bits: fma32 must equal a*b + c rounded once (exact rationals, ties to even)."""
-    rng = np.random.default_rng(21)
-    trips = []
-    for gap in (0, 8, 24, 30, 40):
-        a = rng.standard_normal(400).astype(np.float32)
-        b = rng.standard_normal(400).astype(np.float32)
-        c = (rng.standard_normal(400) * 2.0 ** gap).astype(np.float32)
-        trips += list(zip(a, b, c))
-    a = (rng.integers(1, 256, 2000) * 2.0 ** -7).astype(np.float32)    # 8-bit values
-    b = (rng.integers(1, 256, 2000) * 2.0 ** -9).astype(np.float32)
-    c = (rng.integers(-2 ** 20, 2 ** 20, 2000) * 2.0 ** -12).astype(np.float32)
-    trips += list(zip(a, b, c))
-    A, B, Cc = (np.array(v, dtype=np.float32) for v in zip(*trips))
-    got = O.fma32(A, B, Cc)
-    for x, y, z, g in zip(A, B, Cc, got):
-        want = _round_f32_exact(Fraction(float(x)) * Fraction(float(y)) + Fraction(float(z)))
-        assert g == want, (x, y, z, g, want)
+def _round_bf16_exact(fr):
+    """Nearest bfloat16 to the rational fr, ties to even, by exact comparison (normal range)."""
+    if fr == 0:
+        return 0.0
+    sign = -1 if fr < 0 else 1
+    a = abs(fr)
+    e = math.floor(math.log2(a))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = Fraction(2) ** (e - 7)                     # spacing of bf16 numbers in [2^e, 2^(e+1))
+    k = a / q
+    lo = math.floor(k)
+    rem = k - lo
+    k = lo + 1 if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1) else lo
+    return sign * float(k * q)
 
 
-def test_fma32_tie_broken_by_lost_bits():
-    """a*b + c = (2^40 + 2^17 + 2^16) - 2^-30: the float64 sum lands exactly on the float32 tie
-    and rounding it again would go to even (2^40 + 2^18); the exact value is below the tie."""
-    a = np.float32(2.0 ** 8 * (1 + 2.0 ** -23))
-    b = np.float32(2.0 ** 8 * (1 - 2.0 ** -23))
-    c = np.float32(2.0 ** 40 + 2.0 ** 17)
-    assert np.float32(np.float64(a) * np.float64(b) + np.float64(c)) == np.float32(2.0 ** 40 + 2.0 ** 18)
-    assert O.fma32(a, b, c) == np.float32(2.0 ** 40 + 2.0 ** 17)
-    assert O.fma32(-a, b, -c) == -np.float32(2.0 ** 40 + 2.0 ** 17)
+def _f32_sum_in_order(terms):
+    """Float32 evaluation of sum(terms) in the given order, every addition rounded once."""
+    acc = terms[0]
+    for t in terms[1:]:
+        acc = Fraction(float(_round_f32_exact(acc + t)))
+    return acc
+
+
+def _hc_post_exact(X, F, u, C, k, i):
+    """X'_k at feature i by exact rationals: float32-rounded products, float32 sums over j in
+    index order, the rounded sublayer product added last, one bf16 rounding."""
+    prods = [Fraction(float(_round_f32_exact(Fraction(C[j, k]) * Fraction(X[j, i]))))
+             for j in range(X.shape[0])]
+    s = _f32_sum_in_order(prods)
+    uf = Fraction(float(_round_f32_exact(Fraction(u[k]) * Fraction(F[i]))))
+    return _round_bf16_exact(Fraction(float(_round_f32_exact(uf + s))))
+
+
+def test_hc_post_hc_pre_float32_brute_force():
+    """hc_post and hc_pre against an exact-rational evaluation of the pages' float32 arithmetic
+    (Stream weights for the feed-forward, Code: hc_post, hc_pre: each product a float32 tensor,
+    summed over the stream index, cast to bf16): float32 weights with full 24-bit mantissas, so
+    most products need rounding."""
+    rng = np.random.default_rng(31)
+    N, n, d = 3, 4, 24
+    X, F = _rand_streams(N, n, d, 32)
+    u = rng.uniform(0, 2, (N, n)).astype(np.float32).astype(np.float64)
+    C = rng.uniform(0, 1, (N, n, n)).astype(np.float32).astype(np.float64)
+    p = rng.uniform(0, 1, (N, n)).astype(np.float32).astype(np.float64)
+    Xp = O.hc_post(X, F, u, C)
+    Xr = O.hc_post(X, F, u, C, comb_row_dest=True)
+    yh = O.hc_pre(Xp, p)
+    for t in range(N):
+        for i in range(d):
+            for k in range(n):
+                assert Xp[t, k, i] == _hc_post_exact(X[t], F[t], u[t], C[t], k, i)
+                assert Xr[t, k, i] == _hc_post_exact(X[t], F[t], u[t], C[t].T, k, i)
+            prods = [Fraction(float(_round_f32_exact(Fraction(p[t, j]) * Fraction(Xp[t, j, i]))))
+                     for j in range(n)]
+            assert yh[t, i] == _round_bf16_exact(_f32_sum_in_order(prods))
+
+
+def test_hc_products_rounded_before_the_sum():
+    """A product that float32 rounds down onto a bf16 tie once added: y_hat = p_0 X'_0 + p_1 X'_1
+    with p_0 X'_0 = 2^-24 exact and p_1 X'_1 = A in (1 + 2^-8, 1 + 2^-8 + 2^-24). Rounding A
+    first gives 1 + 2^-8, plus 2^-24 is a float32 tie that stays there, a bf16 tie that goes to
+    even: 1. A fused multiply-add would keep A's low bits and give 1 + 2^-7."""
+    cases = 0
+    for m in range(1, 128):
+        x1 = 1.0 + m / 128.0                                   # a bf16 value
+        lo = Fraction(1) + Fraction(1, 2 ** 8)
+        c = np.float32(float((lo + Fraction(1, 2 ** 25)) / Fraction(x1)))
+        for p1 in (c, np.nextafter(c, np.float32(2)), np.nextafter(c, np.float32(0))):
+            A = Fraction(float(p1)) * Fraction(x1)
+            if lo < A < lo + Fraction(1, 2 ** 24):
+                break
+        else:
+            continue
+        Xp = np.zeros((1, 4, 1))
+        Xp[0, 0, 0], Xp[0, 1, 0] = 1.0, x1
+        pre = np.array([[2.0 ** -24, float(p1), 0.0, 0.0]])
+        assert O.hc_pre(Xp, pre)[0, 0] == 1.0
+        assert _round_bf16_exact(Fraction(float(_round_f32_exact(A + Fraction(1, 2 ** 24))))) == 1.0 + 2.0 ** -7
+        # the same in hc_post, once through comb (C_0k X_0 + C_1k X_1) and once through the
+        # sublayer term (u_k F + C_0k X_0)
+        X = np.zeros((1, 4, 1))
+        X[0, 0, 0], X[0, 1, 0] = 1.0, x1
+        C = np.zeros((1, 4, 4))
+        C[0, 0, 2], C[0, 1, 2] = 2.0 ** -24, float(p1)
+        assert O.hc_post(X, np.zeros((1, 1)), np.zeros((1, 4)), C)[0, 2, 0] == 1.0
+        C[0, 1, 2] = 0.0
+        u = np.array([[0.0, 0.0, float(p1), 0.0]])
+        assert O.hc_post(X, np.full((1, 1), x1), u, C)[0, 2, 0] == 1.0
+        cases += 1
+    assert cases > 10
+
+
+def test_hc_sums_run_in_stream_order():
+    """Exact products (X' = 1, weights of few bits) whose float32 sum depends on the order of
+    the additions: the oracle follows index order j = 0..3 in hc_pre, and in hc_post adds the
+    sublayer term last. The set of cases includes ones where pairwise and reversed orders, and
+    adding the sublayer term first, all round differently."""
+    vals = [1.0, 2.0 ** -8, 2.0 ** -24, 1.5 * 2.0 ** -24, 2.0 ** -23, -2.0 ** -24, 3.0 * 2.0 ** -9]
+    rng = np.random.default_rng(33)
+    picks = rng.choice(len(vals), size=(600, 5))
+    diff_pw = diff_rev = diff_first = 0
+
+    def bf(terms):
+        return _round_bf16_exact(_f32_sum_in_order([Fraction(v) for v in terms]))
+    for row in picks:
+        q = [vals[i] for i in row]
+        Xp = np.ones((1, 4, 1))
+        got = O.hc_pre(Xp, np.array([q[:4]]))[0, 0]
+        want = bf(q[:4])
+        assert got == want
+        pw = _round_bf16_exact(Fraction(float(_round_f32_exact(
+            Fraction(float(_round_f32_exact(Fraction(q[0]) + Fraction(q[1])))) +
+            Fraction(float(_round_f32_exact(Fraction(q[2]) + Fraction(q[3]))))))))
+        diff_pw += pw != want
+        diff_rev += bf(q[3::-1]) != want
+        # hc_post with F = 1, u_k = q[4], C_jk = q[j]: the sublayer term is added last
+        X = np.ones((1, 4, 1))
+        C = np.zeros((1, 4, 4))
+        C[0, :, 0] = q[:4]
+        u = np.array([[q[4], 0.0, 0.0, 0.0]])
+        post = O.hc_post(X, np.ones((1, 1)), u, C)[0, 0, 0]
+        assert post == _round_bf16_exact(Fraction(float(_round_f32_exact(
+            Fraction(q[4]) + _f32_sum_in_order([Fraction(v) for v in q[:4]])))))
+        diff_first += post != bf([q[4]] + q[:4])
+    assert diff_pw > 0 and diff_rev > 0 and diff_first > 0
 
 
 # ---------------------------------------------------------------------------------------------
