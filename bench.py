@@ -52,7 +52,7 @@ def measured_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("fused.cu", "ptx.cuh", "mix_math.cuh", "layout.cuh"):
+    for f in ("fused.cu", "ptx.cuh", "mix_math.cuh", "hc_arith.cuh", "layout.cuh"):
         with open(os.path.join(ROOT, "stream_residual_fusion_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -84,10 +84,12 @@ size_t mhc_workspace_bytes(int n, int d);
  *   post = 2 sigmoid(scale[1] m[n:2n] + base[n:2n])                          -> post_out
  *   comb = Sinkhorn(softmax_k(scale[2] m[2n:] + base[2n:]) ), sinkhorn_iters rounds -> comb_out
  *   y    = RMSNorm(hc_pre(X', pre_prev); gain, norm_eps)                     -> y_out (bf16)
- * hc_post and hc_pre are evaluated in float32 (Code: hc_post, hc_pre) as chains of fused
- * multiply-adds over the stream index, left to right, then rounded to bf16:
- *   X'_k  = fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0))))
- *   y_hat = fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0)))
+ * hc_post and hc_pre are evaluated in float32 as the pages' code spells them out (Code:
+ * hc_post, hc_pre: every product a float32 tensor, summed over the stream index), each product
+ * and each addition rounded to float32, the sums in stream order, then rounded to bf16
+ * (fl = one float32 rounding):
+ *   X'_k  = fl(u_k F) + (((fl(C_0k X_0) + fl(C_1k X_1)) + fl(C_2k X_2)) + fl(C_3k X_3))
+ *   y_hat = ((fl(p_0 X'_0) + fl(p_1 X'_1)) + fl(p_2 X'_2)) + fl(p_3 X'_3)
  *
  *   X         bf16 [N, n, d]      residual streams                      (read once)
  *   F         bf16 [N, d]         sublayer output                        (read once)

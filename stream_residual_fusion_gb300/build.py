@@ -15,11 +15,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmhc.so")
 SOURCES = ["fused.cu", "small.cu", "abi.cu", "host_pipeline.cu"]
-HEADERS = ["ptx.cuh", "mix_math.cuh", "internal.h", "layout.cuh"]
+HEADERS = ["ptx.cuh", "mix_math.cuh", "hc_arith.cuh", "internal.h", "layout.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: a separate float32 multiply and add must stay two roundings (hc_post and hc_pre
-# are defined with float32 products and float32 sums); explicit fma instructions are unaffected.
+# are defined with float32 products and float32 sums; their kernels also spell the products and
+# sums out as explicit round-to-nearest PTX); explicit fma instructions are unaffected.
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xptxas=--fmad=false",
           "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
           f"-I{INCLUDE}", f"-I{CSRC}"]

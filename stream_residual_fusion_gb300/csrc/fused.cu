@@ -44,6 +44,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "hc_arith.cuh"
 #include "layout.cuh"
 #include "mix_math.cuh"
 #include "ptx.cuh"
@@ -714,21 +715,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int j = 0; j < 4; ++j) x[j] = bf2_to_f2(xw[j][w]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  // X'_k = fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0))))
-                  f2 mixed = mul2(cc[0][k], x[0]);
-                  mixed = fma2(cc[1][k], x[1], mixed);
-                  mixed = fma2(cc[2][k], x[2], mixed);
-                  mixed = fma2(cc[3][k], x[3], mixed);
-                  ow[k][w] = f2_to_bf2(fma2(cu[k], f, mixed));
+                  // X'_k: rounded products summed in stream order (hc_arith.cuh)
+                  const f2 ck[4] = {cc[0][k], cc[1][k], cc[2][k], cc[3][k]};
+                  ow[k][w] = f2_to_bf2(hc_post_pair(ck, cu[k], x, f));
                   xp[k] = bf2_to_f2(ow[k][w]);
                   lx = fma2(xp[k], xp[k], lx);
                 }
-                // y_hat = fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0)))
-                f2 yh = mul2(cp[0], xp[0]);
-                yh = fma2(cp[1], xp[1], yh);
-                yh = fma2(cp[2], xp[2], yh);
-                yh = fma2(cp[3], xp[3], yh);
-                ywall[4 * q + w] = f2_to_bf2(yh);
+                ywall[4 * q + w] = f2_to_bf2(hc_pre_pair(cp, xp));
                 const f2 yr = bf2_to_f2(ywall[4 * q + w]);
                 ly = fma2(yr, yr, ly);
               }

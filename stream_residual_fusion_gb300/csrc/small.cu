@@ -2,6 +2,7 @@
 // one-op-per-kernel hc_post / hc_pre of the unfused form.
 #include <cuda_runtime.h>
 
+#include "hc_arith.cuh"
 #include "internal.h"
 #include "layout.cuh"
 #include "mix_math.cuh"
@@ -171,8 +172,8 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_row_kernel(const uint4* _
   }
 }
 
-// hc_post alone: one thread per 8 columns of one token, all 4 streams (same float32 order as
-// the fused kernel: X'_k = fma(u_k, F, fma(C_3k, X_3, fma(C_2k, X_2, fma(C_1k, X_1, C_0k X_0))))).
+// hc_post alone: one thread per 8 columns of one token, all 4 streams (the float32 evaluation of
+// hc_arith.cuh, as in the fused kernel).
 __global__ void hc_post_kernel(const uint4* __restrict__ X, const uint4* __restrict__ F,
                                const float* __restrict__ post, const float* __restrict__ comb,
                                uint4* __restrict__ Xo, int64_t N, int d, int row_dest) {
@@ -210,11 +211,8 @@ __global__ void hc_post_kernel(const uint4* __restrict__ X, const uint4* __restr
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        f2 mixed = mul2(cc[0][k], x[0]);
-        mixed = fma2(cc[1][k], x[1], mixed);
-        mixed = fma2(cc[2][k], x[2], mixed);
-        mixed = fma2(cc[3][k], x[3], mixed);
-        ow[k][w] = f2_to_bf2(fma2(cu[k], f, mixed));
+        const f2 ck[4] = {cc[0][k], cc[1][k], cc[2][k], cc[3][k]};
+        ow[k][w] = f2_to_bf2(hc_post_pair(ck, cu[k], x, f));
       }
     }
 #pragma unroll
@@ -222,7 +220,7 @@ __global__ void hc_post_kernel(const uint4* __restrict__ X, const uint4* __restr
   }
 }
 
-// hc_pre alone: y_hat = bf16(fma(p_3, X'_3, fma(p_2, X'_2, fma(p_1, X'_1, p_0 X'_0)))).
+// hc_pre alone: y_hat = bf16 of the float32 evaluation of hc_arith.cuh.
 __global__ void hc_pre_kernel(const uint4* __restrict__ Xp, const float* __restrict__ pre,
                               uint4* __restrict__ y, int64_t N, int d) {
   const int chunks = d / 8;
@@ -248,11 +246,7 @@ __global__ void hc_pre_kernel(const uint4* __restrict__ Xp, const float* __restr
         const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
         x[j] = bf2_to_f2(xw[w]);
       }
-      f2 yh = mul2(cp[0], x[0]);
-      yh = fma2(cp[1], x[1], yh);
-      yh = fma2(cp[2], x[2], yh);
-      yh = fma2(cp[3], x[3], yh);
-      o[w] = f2_to_bf2(yh);
+      o[w] = f2_to_bf2(hc_pre_pair(cp, x));
     }
     y[t * chunks + c] = make_uint4(o[0], o[1], o[2], o[3]);
   }

@@ -1,8 +1,9 @@
 """Comparison rules for the CUDA path against the CPU oracle.
 
 Tolerances (stated once, used by every GPU test):
-  * X' and y_hat: bit-exact. Both sides evaluate the same float32 operations in the same order
-    before the bf16 rounding, so the rounding decision is identical.
+  * X' and y_hat: bit-exact. The pages' code fixes the float32 arithmetic before the bf16
+    rounding (each product rounded, the products summed over the stream index in order), and
+    both sides evaluate exactly that, so the rounding decision is identical.
   * y: within 2 bf16 ulps of the oracle (the RMS statistic is summed in a different order).
   * p, u, C: absolute error <= 1e-5.
   * m (the 24 mix numbers): per token, max |dm| <= 1e-4 * max |m|.
