@@ -153,9 +153,9 @@ int mhc_fused_step_mxfp8(const void* X, const void* F, const float* pre_prev,
 
 /* ---- the fused step without any allocation --------------------------------------------------
  * No counterpart in the paper: an addition for callers that cannot allocate device memory when
- * they run the step (code being captured into a CUDA graph or stream that must not allocate, a
- * serving loop with a fixed memory budget or an allocator it cannot call, a plain C host with no
- * allocator of its own). Same arguments and results as mhc_fused_step, without the workspace:
+ * they run the step -- a serving loop that runs under a fixed device-memory budget, or whose
+ * caching allocator it may not enter from that point, or a plain C host that links this library
+ * and has no device allocator of its own. Same arguments and results as mhc_fused_step, without the workspace:
  * the packed weights and the step scratch live in one fixed array of
  * mhc_noalloc_scratch_bytes() (8 MiB) that the library keeps on every GPU that loads it until
  * the process exits. No device memory is allocated or freed, by this call or by anything it

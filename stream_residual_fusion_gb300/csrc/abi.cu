@@ -373,10 +373,9 @@ int mhc_step_config(int64_t N, int n, int d, unsigned flags, int* split, int* ti
 // ---------------------------------------------------------------------------------------------
 // Allocation-free fused step.
 //
-// Some callers cannot allocate device memory at the point they run the step: code inside a
-// CUDA-graph or stream capture that must not allocate, a serving loop running under a fixed
-// memory budget or a caching allocator it cannot enter, or a plain C host that links this
-// library and has no allocator of its own. This entry point runs the same fused step with its
+// Some callers cannot allocate device memory at the point they run the step: a serving loop
+// running under a fixed device-memory budget, or one whose caching allocator it may not enter
+// there, or a plain C host that links this library and has no device allocator of its own. This entry point runs the same fused step with its
 // scratch (the packed weights and the step's exchange area) in one fixed array that the
 // library holds on every GPU that loads it, until the process exits.
 

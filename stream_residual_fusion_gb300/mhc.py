@@ -16,7 +16,9 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmhc.so")
+# MHC_LIBRARY names another build of the same ABI (for example the bounds-checked build,
+# libmhc_checked.so); the import fails if that file is missing too.
+LIB_PATH = os.environ.get("MHC_LIBRARY") or os.path.join(_PKG, "libmhc.so")
 
 MHC_OK = 0
 MHC_ERR_NULL = -1

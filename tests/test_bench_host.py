@@ -1,5 +1,7 @@
 """Host-side pieces of bench.py (no GPU): the algorithmic byte counts it reports, checked against
 the oracle's pinned traffic counts, and the lookup of the committed ncu traffic summary."""
+import pytest
+
 import bench
 import oracle as O
 
@@ -33,3 +35,11 @@ def test_ncu_traffic_lookup(tmp_path, monkeypatch):
     assert bench.ncu_traffic(10) is None
     summary.unlink()
     assert bench.ncu_traffic(10) is None
+
+
+def test_percentile_interpolates_between_ranks():
+    xs = [float(i) for i in range(1, 201)]            # 200 launches: 1.0 .. 200.0 ms
+    assert bench.percentile(xs, 50) == pytest.approx(100.5)
+    assert bench.percentile(xs, 99) == pytest.approx(198.01)
+    assert bench.percentile(xs, 0) == 1.0 and bench.percentile(xs, 100) == 200.0
+    assert bench.percentile([3.0], 95) == 3.0 and bench.percentile([], 50) is None

@@ -1,12 +1,13 @@
 """Parity of the fused single-pass mHC step (mhc_fused_step / mhc_fused_step_packed) with the
 CPU oracle: several tiles with a ragged tail, every width split, both readings of comb, in place,
-edge cases, the bounded-wait status path, and the benchmark workloads (in full where the oracle
-finishes in seconds, else on sampled tokens plus properties that hold at any size)."""
+edge cases, the bounded-wait status path, and the five benchmark workloads, every token of each
+compared with the oracle (the two largest in chunks on a process pool)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
+from tests.oracle_pool import full_parity
 from tests.parity import (TOL_PUC, assert_abs, assert_bf16_within, assert_exact, check_step,
                           oracle_step, to64)
 
@@ -148,15 +149,6 @@ def test_unfused_chain_matches(M, synth):
 # the benchmark workloads
 
 
-def _sample(N, outliers=None, k=384, seed=0):
-    rng = np.random.default_rng(seed)
-    picks = set(range(min(N, 130))) | set(range(max(0, N - 130), N))
-    picks |= set(rng.choice(N, size=min(N, k), replace=False).tolist())
-    if outliers is not None:
-        picks |= set(outliers.tolist())
-    return torch.tensor(sorted(picks), dtype=torch.long)
-
-
 @pytest.mark.parametrize("name", ["tiny", "prefill4k", "decode256"])
 def test_workload_full(M, synth, name):
     w = synth.WORKLOADS[name]
@@ -168,23 +160,21 @@ def test_workload_full(M, synth, name):
 
 
 @pytest.mark.parametrize("name", ["prefill32k", "prefill128k"])
-def test_workload_sampled(M, synth, name):
+def test_workload_full_chunked(M, synth, name):
+    """The two large workloads at full size, in the bench's launch configuration: every token
+    against the oracle (chunks on a spawned process pool, tests/oracle_pool.py), every outlier
+    token of the B=8, T=16384 batch included, plus properties that hold for every token."""
     w = synth.WORKLOADS[name]
     inp = synth.make_workload(w, seed=1, device=DEV)
+    inp.pop("outliers", None)
     out = _run(M, inp)
     assert M.get_status() == M.MHC_OK
-    # properties that hold for every token
     for k in ("Xp", "y", "pre", "post", "comb", "mixes"):
         assert torch.isfinite(out[k].float()).all(), k
     col = out["comb"].sum(dim=1)
     assert (col <= 1.0 + 1e-5).all() and (out["comb"] > 0).all()
     assert ((out["post"] >= 0) & (out["post"] <= 2)).all()   # 2*sigmoid saturates in fp32
-    # sampled tokens against the oracle, every outlier token included
-    idx = _sample(w.N, inp.get("outliers", None) if "outliers" in inp else None)
-    sub = synth.subset({k: v for k, v in inp.items()}, idx.to(DEV))
-    ref = oracle_step(sub)
-    got = {k: v[idx.to(DEV)] for k, v in out.items()}
-    check_step(got, ref)
+    assert full_parity(inp, out) == w.N
 
 
 @pytest.mark.parametrize("N,d,tile", [

@@ -2,12 +2,13 @@
 and the mix numbers bit-identical to the bf16-y step; the E8M0 scales and E4M3 codes against the
 oracle's encoding of its bf16 y (oracle.mx), and, as a property of the kernel, equal to a library
 MXFP8 cast of the kernel's own bf16 y; over several tiles with a ragged tail, the width splits,
-short tiles, an all-zero token, power-of-two rescaling and the benchmark workload on sampled
-tokens."""
+short tiles, an all-zero token, power-of-two rescaling and every token of the benchmark
+workload."""
 import numpy as np
 import pytest
 import torch
 
+from tests.oracle_pool import full_parity
 from tests.parity import check_mxfp8, check_step, oracle_step, to64
 
 pytestmark = pytest.mark.gpu
@@ -117,9 +118,9 @@ def test_mxfp8_zero_and_wide_range_tokens(M, synth):
         assert torch.equal(q2["y_scale"].long()[nz], q["y_scale"].long()[nz] + shift)
 
 
-def test_mxfp8_workload_sampled(M, synth):
-    """The B=4, T=8192 workload: every token equal to the cast of the kernel's bf16 y, sampled
-    tokens (the first and last tiles among them) against the oracle, no NaN code."""
+def test_mxfp8_workload_full(M, synth):
+    """The B=4, T=8192 workload: every token equal to the cast of the kernel's bf16 y and, in
+    chunks on a process pool, against the oracle; no NaN code."""
     w = synth.WORKLOADS["prefill32k"]
     inp = synth.make_workload(w, seed=1, device=DEV)
     inp.pop("outliers", None)
@@ -134,11 +135,4 @@ def test_mxfp8_workload_sampled(M, synth):
     codes = q["y_codes"]
     assert not ((codes & 0x7F) == 0x7F).any()          # no NaN codes
     assert (q["y_scale"] <= 254).all()
-    rng = np.random.default_rng(3)
-    idx = sorted(set(range(130)) | set(range(w.N - 130, w.N)) |
-                 set(rng.choice(w.N, 256, replace=False).tolist()))
-    idx = torch.tensor(idx, dtype=torch.long, device=DEV)
-    sub = synth.subset(inp, idx)
-    ref = oracle_step(sub)
-    check_mxfp8(codes[idx].cpu().numpy(), q["y_scale"][idx].cpu().numpy(), ref["y"])
-    assert to64(q["pre"][idx]).shape == ref["pre"].shape
+    assert full_parity(inp, q) == w.N                 # every token against the oracle
