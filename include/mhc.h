@@ -39,6 +39,8 @@ extern "C" {
 #define MHC_ERR_CUDA      -5  /* a CUDA runtime/driver call failed (launch, tensor map, attribute) */
 #define MHC_ERR_TIMEOUT   -6  /* a device-side bounded wait gave up (see mhc_get_status)         */
 #define MHC_ERR_WORKSPACE -7  /* workspace missing or smaller than *_workspace_bytes()           */
+#define MHC_ERR_BOUNDS    -8  /* bounds-checked build only: an index check failed and its access
+                                 was skipped (see mhc_get_status, mhc_checked_build)           */
 
 /* ---- flags ------------------------------------------------------------------------------- */
 /* Reading of comb in hc_post. Default (0): the pages' code, X'_k = u_k F + sum_j C_jk X_j
@@ -49,6 +51,10 @@ extern "C" {
 /* Test hook: one thread per CTA waits on a barrier that nothing completes, with a ~2 ms limit;
  * the wait gives up, records MHC_ERR_TIMEOUT for mhc_get_status, and the call completes.      */
 #define MHC_DEBUG_NEVER_ARRIVE   0x2u
+/* Test hook of the bounds-checked build only (MHC_ERR_SHAPE in other builds): one finisher
+ * store and one MXFP8 scale store of the first CTA get a row index N rows past the end; the
+ * index checks skip both and mhc_get_status reports MHC_ERR_BOUNDS.                          */
+#define MHC_DEBUG_PLANT_OOB      0x4u
 /* Bits 8..11: log2 + 1 of the number of CTAs (1, 2, 4, 8, 16 or 32) that split the width d of
  * each token tile between them (a group of co-resident CTAs); values above 6 are MHC_ERR_SHAPE.
  * 0 = automatic: with the tile height (below), the shape that minimises the busiest group's
@@ -259,10 +265,15 @@ int mhc_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int n, 
 int mhc_pack_weights(const float* W_mix, void* W_packed, int n, int d, void* stream);
 
 /* ---- status --------------------------------------------------------------------------------
- * Synchronises `stream`, then returns and clears the device status word: MHC_OK, or
- * MHC_ERR_TIMEOUT if a bounded device-side wait gave up since the last call, or MHC_ERR_CUDA
- * if the synchronisation itself failed.                                                       */
+ * Synchronises `stream`, then returns and clears the device status word: MHC_OK,
+ * MHC_ERR_BOUNDS if an index check of the bounds-checked build failed since the last call,
+ * else MHC_ERR_TIMEOUT if a bounded device-side wait gave up, or MHC_ERR_CUDA if the
+ * synchronisation itself failed.                                                              */
 int mhc_get_status(void* stream);
+/* 1 for the bounds-checked build of the library (libmhc_checked.so: every copy, store and
+ * exchange access of the fused step tests its index first and skips it on failure, reporting
+ * MHC_ERR_BOUNDS), 0 for the regular build (the tests compiled away).                          */
+int mhc_checked_build(void);
 /* Launch shape of the fused step (and of mhc_mixes) for N tokens of width d with `flags` on
  * the current device: CTAs that share a tile, tokens per tile, and groups launched (each group
  * is `split` CTAs, one per SM). Diagnostic; needs a GPU.                                      */
@@ -277,7 +288,7 @@ int mhc_step_config(int64_t N, int n, int d, unsigned flags, int* split, int* ti
 int mhc_set_trace(void* buffer, int64_t bytes);
 /* Static text for a status code.                                                              */
 const char* mhc_strerror(int code);
-/* Library ABI version (major*100 + minor).                                                    */
+/* Library ABI version (major*100 + minor): 101.                                               */
 int mhc_version(void);
 
 #ifdef __cplusplus

@@ -52,6 +52,7 @@ namespace {
 // Checks shared by the fused step and the mixes call. Returns MHC_OK and the split, or a code.
 int check_step_shape(int64_t N, int n, int d, int iters, unsigned flags, int* split) {
   if (n != 4 || N < 0 || N > kMaxTokens || iters < 1 || d <= 0) return MHC_ERR_SHAPE;
+  if (!MHC_CHECKED && (flags & FLAG_PLANT_OOB) != 0) return MHC_ERR_SHAPE;   // checked build only
   const int fs = split_flag_value(flags), ft = tile_flag(flags);
   if (fs < 0 || ft < 0) return MHC_ERR_SHAPE;
   *split = choose_split(d, fs);
@@ -339,6 +340,7 @@ int mhc_get_status(void* stream) {
     const unsigned zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MHC_ERR_CUDA;
   }
+  if (v & STATUS_BOUNDS) return MHC_ERR_BOUNDS;
   return (v & STATUS_TIMEOUT) ? MHC_ERR_TIMEOUT : MHC_OK;
 }
 
@@ -352,6 +354,7 @@ const char* mhc_strerror(int code) {
     case MHC_ERR_CUDA: return "a CUDA call failed";
     case MHC_ERR_TIMEOUT: return "a device-side bounded wait gave up";
     case MHC_ERR_WORKSPACE: return "workspace missing or too small";
+    case MHC_ERR_BOUNDS: return "an index check of the bounds-checked build failed (access skipped)";
     default: return "unknown status code";
   }
 }
@@ -442,6 +445,8 @@ int mhc_set_trace(void* buffer, int64_t bytes) {
   return MHC_OK;
 }
 
-int mhc_version(void) { return 100; }
+int mhc_version(void) { return 101; }
+
+int mhc_checked_build(void) { return MHC_CHECKED; }
 
 }  // extern "C"

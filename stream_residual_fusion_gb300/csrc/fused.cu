@@ -154,6 +154,7 @@ struct StepParams {
   unsigned long long* trace;   // optional: 8 phase timestamps per (tile, CTA) (mhc_set_trace)
   unsigned* counters;          // per group: syready[2], pready[2], pfree[2] (zeroed per launch)
   float* gpart;                // per group: [2 buffers][split ranks][TT tokens][PART_STRIDE]
+  const float* gpart_end;      // end of the exchange area (bounds of the checked build)
   int N;
   int tt;                      // tokens per tile (a multiple of 8, <= TT); rows >= tt are idle
   int d;
@@ -165,6 +166,35 @@ struct StepParams {
   float norm_eps;
   unsigned flags;
 };
+
+// Bounds checks of the checked build (MHC_CHECKED=1): the producer's copies, the X'/y stores,
+// the exchange-area accesses, the finisher's stores and the MXFP8 scale stores test their
+// indexes first; a failed test records STATUS_BOUNDS for mhc_get_status and the access is
+// skipped (never a trap). Other builds compile the tests away.
+__device__ __forceinline__ bool checked(bool ok, unsigned* status) {
+#if MHC_CHECKED
+  if (!ok) atomicOr(status, STATUS_BOUNDS);
+  return ok;
+#else
+  (void)status;
+  (void)ok;
+  return true;
+#endif
+}
+// n floats at p lie inside the exchange area.
+__device__ __forceinline__ bool in_gpart(const StepParams& P, const float* p, int n) {
+  return p >= P.gpart && p + n <= P.gpart_end;
+}
+// Row offset planted by FLAG_PLANT_OOB (checked builds only): N rows past the end.
+__device__ __forceinline__ int planted_rows(const StepParams& P, bool here) {
+#if MHC_CHECKED
+  return here && (P.flags & FLAG_PLANT_OOB) != 0 ? P.N : 0;
+#else
+  (void)P;
+  (void)here;
+  return 0;
+#endif
+}
 
 // Fold accumulation group `gg` (TMEM accumulator gg & 1) into this thread's 12 running sums
 // (the tile's first group sets them).
@@ -394,11 +424,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!mbar_wait(&empty[b], ((gs / NSTAGE) - 1) & 1, limit())) timed_out = true;
           }
           const int i0 = col0 + s * cstride;
-          mbar_arrive_expect_tx(&full[b], bytes);
+          if (checked(i0 >= 0 && i0 + DC <= d && t0 >= 0 && t0 < P.N, P.status)) {
+            mbar_arrive_expect_tx(&full[b], bytes);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tma_load_3d_hint(sm + xtile(b, k), &tm_x, &full[b], i0, k, t0, stream_pol);
-          if (FUSED) tma_load_2d_hint(sm + ftile(b), &tm_f, &full[b], i0, t0, stream_pol);
+            for (int k = 0; k < 4; ++k)
+              tma_load_3d_hint(sm + xtile(b, k), &tm_x, &full[b], i0, k, t0, stream_pol);
+            if (FUSED) tma_load_2d_hint(sm + ftile(b), &tm_f, &full[b], i0, t0, stream_pol);
+          } else {
+            mbar_arrive(&full[b]);      // the slot completes without data
+          }
         }
         if (auto tr = trace_rec(tile)) tr[1] = global_timer_ns();
       }
@@ -427,6 +461,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int t0 = tile * tt;
         const uint32_t cnt = static_cast<uint32_t>(min(tt, P.N - t0));
         uint8_t* buf = sm + OFF_PART + (it_ & 1) * RUN_BYTES;
+        if (!checked(t0 >= 0 && cnt >= 1 && cnt <= static_cast<uint32_t>(TT) &&
+                     t0 + static_cast<int>(cnt) <= P.N, P.status)) {
+          mbar_arrive(&cfull[it_ & 1]);
+          return;
+        }
         mbar_arrive_expect_tx(&cfull[it_ & 1], cnt * 96u);
         bulk_load_hint(buf, P.post_prev + static_cast<size_t>(t0) * 4, cnt * 16u, &cfull[it_ & 1], coef_pol);
         bulk_load_hint(buf + COEF_PRE, P.pre_prev + static_cast<size_t>(t0) * 4, cnt * 16u, &cfull[it_ & 1], coef_pol);
@@ -466,6 +505,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int e = u % NW;
         const int slot_in_tile = (u / HALVES) % S;
         const int blk = (col0 + slot_in_tile * cstride) / WDC + u % HALVES;
+        if (!checked(blk >= 0 && (blk + 1) * WDC <= d, P.status)) {
+          mbar_arrive(&wfull[e]);
+          return;
+        }
         mbar_arrive_expect_tx(&wfull[e], STEP_WBLOCK_BYTES);
         bulk_load_hint(sm + wtile(e, 0), P.w_packed + static_cast<size_t>(blk) * STEP_WBLOCK_BYTES,
                        STEP_WBLOCK_BYTES, &wfull[e], weight_pol);
@@ -524,16 +567,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int b = gs % NSTAGE;
           if (!mbar_wait(&xready[b], (gs / NSTAGE) & 1, limit())) timed_out = true;
           const int i0 = col0 + s * cstride;
+          if (checked(i0 >= 0 && i0 + DC <= d && t0 >= 0 && t0 < P.N, P.status)) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tma_store_3d_hint(&tm_xo, sm + xtile(b, k), i0, k, t0, stream_pol);
+            for (int k = 0; k < 4; ++k) tma_store_3d_hint(&tm_xo, sm + xtile(b, k), i0, k, t0, stream_pol);
+          }
           if (gs >= R) {
             // the y the consumers normalised into the F tile: global slot gs - R
             const int src = gs - R;
             const int ytile = c0 + (src / S) * nclust;
-            if constexpr (MX)
-              store_codes(&tm_y, &tm_y8, sm + ftile(b), col0 + (src % S) * cstride, ytile * tt, tt, stream_pol);
-            else
-              tma_store_2d_hint(&tm_y, sm + ftile(b), col0 + (src % S) * cstride, ytile * tt, stream_pol);
+            const int ycol = col0 + (src % S) * cstride;
+            if (checked(ycol >= 0 && ycol + DC <= d && ytile >= 0 && ytile * tt < P.N, P.status)) {
+              if constexpr (MX)
+                store_codes(&tm_y, &tm_y8, sm + ftile(b), ycol, ytile * tt, tt, stream_pol);
+              else
+                tma_store_2d_hint(&tm_y, sm + ftile(b), ycol, ytile * tt, stream_pol);
+            }
           }
           bulk_commit();
           bulk_wait_read<0>();          // the slot's tiles have been read: free the slot
@@ -606,6 +654,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           rms_v[u] = 0.f;
           if (rk0 + u < split) {
             const float* row = gpart(it_ & 1, rk0 + u) + tl * PART_STRIDE + 24 + TPT;
+            if (!checked(in_gpart(P, row, TPT), P.status)) continue;
             if constexpr (TPT == 4) {
               const float4 q4 = __ldcg(reinterpret_cast<const float4*>(row));
               rms_v[u] = (q4.x + q4.y) + (q4.z + q4.w);
@@ -636,9 +685,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // counter's release orders what the warp wrote before __syncwarp)
         float4* dst = reinterpret_cast<float4*>(gpart(it_ & 1, g) + tl * PART_STRIDE + 12 * h);
         const float4* src = reinterpret_cast<const float4*>(run);
-        dst[0] = src[0];
-        dst[1] = src[1];
-        dst[2] = src[2];
+        if (checked(in_gpart(P, reinterpret_cast<const float*>(dst), 12), P.status)) {
+          dst[0] = src[0];
+          dst[1] = src[1];
+          dst[2] = src[2];
+        }
         // the sums buffer is free now: the poster's bulk copy of a later tile's coefficients
         // will write it (async proxy after these generic accesses)
         fence_proxy_async_smem();
@@ -754,8 +805,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const uint32_t code = mx_scale_code(max(e_own, static_cast<uint32_t>(xch[(part ^ 1) * TT + tl])));
               *reinterpret_cast<uint4*>(sm + ftile(b) + code_offset(tl, part)) = mx_encode16(yv, code);
               const int token = s >= RLAG ? ytok1 : ytok2;
-              if (part == 0 && tl < tt && token < P.N)
-                P.y_scale[static_cast<size_t>(token) * (P.d / 32) + ycol / 32] = static_cast<uint8_t>(code);
+              if (part == 0 && tl < tt && token < P.N) {
+                const int row = token + planted_rows(P, blockIdx.x == 0 && tl == 0 && gs == R);
+                if (checked(row >= 0 && row < P.N && ycol >= 0 && ycol + DC <= d, P.status))
+                  P.y_scale[static_cast<size_t>(row) * (P.d / 32) + ycol / 32] = static_cast<uint8_t>(code);
+              }
             } else {
 #pragma unroll
               for (int q = 0; q < CPH; ++q)
@@ -805,8 +859,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (it >= 2 && !mbar_wait(&pfreed[it & 1], ((it >> 1) - 1) & 1, limit())) timed_out = true;
       {
         float* pt = gpart(it & 1, g) + tl * PART_STRIDE;
-        pt[24 + part] = sx2.x + sx2.y;
-        pt[24 + TPT + part] = sy2.x + sy2.y;
+        if (checked(in_gpart(P, pt, PART_STRIDE), P.status)) {
+          pt[24 + part] = sx2.x + sx2.y;
+          pt[24 + TPT + part] = sy2.x + sy2.y;
+        }
       }
       __syncwarp();
       if (FUSED && lane == 0) mbar_arrive(&posted[it & 1]);   // published by the poster (warp 0)
@@ -881,9 +937,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t code = mx_scale_code(max(e_own[e], other));
                 *reinterpret_cast<uint4*>(sm + yslot(src - g0) + code_offset(tl, part)) = mx_encode16(yv[e], code);
                 const int token = (c0 + (src / S) * nclust) * tt + tl;
-                if (part == 0 && tl < tt && token < P.N)
-                  P.y_scale[static_cast<size_t>(token) * (P.d / 32) + (col0 + col[e] * cstride) / 32] =
-                      static_cast<uint8_t>(code);
+                const int scol = col0 + static_cast<int>(col[e]) * cstride;
+                const int row = token + planted_rows(P, blockIdx.x == 0 && tl == 0 && src == first);
+                if (part == 0 && tl < tt && token < P.N &&
+                    checked(row >= 0 && row < P.N && scol >= 0 && scol + DC <= d, P.status))
+                  P.y_scale[static_cast<size_t>(row) * (P.d / 32) + scol / 32] = static_cast<uint8_t>(code);
               }
             }
           }
@@ -907,16 +965,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // four or more stores per staged slot: every consumer warp issues those of every
           // NCONS-th slot (measured 10% faster at 4,096 tokens than one issuing thread)
           if (lane == 0) {
-            for (int src = g0 + (warp - NROLE); src < g1; src += NCONS)
-              store_codes(&tm_y, &tm_y8, sm + yslot(src - g0), col0 + (src % S) * cstride,
-                          (c0 + (src / S) * nclust) * tt, tt, stream_pol);
+            for (int src = g0 + (warp - NROLE); src < g1; src += NCONS) {
+              const int ytile = c0 + (src / S) * nclust;
+              const int ycol = col0 + (src % S) * cstride;
+              if (checked(ycol >= 0 && ycol + DC <= d && ytile >= 0 && ytile * tt < P.N, P.status))
+                store_codes(&tm_y, &tm_y8, sm + yslot(src - g0), ycol, ytile * tt, tt, stream_pol);
+            }
             bulk_commit();
             bulk_wait_read<0>();
           }
         } else if (warp == NROLE && lane == 0) {
           for (int src = g0; src < g1; ++src) {
             const int ytile = c0 + (src / S) * nclust;
-            tma_store_2d_hint(&tm_y, sm + yslot(src - g0), col0 + (src % S) * cstride, ytile * tt, stream_pol);
+            const int ycol = col0 + (src % S) * cstride;
+            if (checked(ycol >= 0 && ycol + DC <= d && ytile >= 0 && ytile * tt < P.N, P.status))
+              tma_store_2d_hint(&tm_y, sm + yslot(src - g0), ycol, ytile * tt, stream_pol);
           }
           bulk_commit();
           bulk_wait_read<0>();
@@ -974,6 +1037,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               for (int o = 0; o < 2; ++o) {
                 const float4* row = reinterpret_cast<const float4*>(
                     gpart(pb, min(rk + o, split - 1)) + tl2[u] * PART_STRIDE);
+                if (!checked(in_gpart(P, reinterpret_cast<const float*>(row), PART_STRIDE), P.status)) {
+                  v[u][o][0] = v[u][o][1] = v[u][o][2] = v[u][o][3] = make_float4(0.f, 0.f, 0.f, 0.f);
+                  continue;
+                }
                 v[u][o][0] = __ldcg(row);
                 v[u][o][1] = __ldcg(row + 1);
                 v[u][o][2] = __ldcg(row + 2 + j);
@@ -1003,13 +1070,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float pj, uj, crow[4];
             split_sinkhorn_row(mrow, m0[j], m1[j], j, __ldg(P.scale), __ldg(P.scale + 1),
                                __ldg(P.scale + 2), P.base, P.iters, P.hc_eps, pj, uj, crow);
-            if (in_range && token2 < P.N) {
-              P.pre_out[static_cast<size_t>(token2) * 4 + j] = pj;
-              P.post_out[static_cast<size_t>(token2) * 4 + j] = uj;
-              reinterpret_cast<float4*>(P.comb_out + static_cast<size_t>(token2) * 16)[j] =
+            const int row = token2 + planted_rows(P, blockIdx.x == 0 && it == 0 && base_t == 0 && u == 0 && q == 0);
+            if (in_range && token2 < P.N && checked(row >= 0 && row < P.N, P.status)) {
+              P.pre_out[static_cast<size_t>(row) * 4 + j] = pj;
+              P.post_out[static_cast<size_t>(row) * 4 + j] = uj;
+              reinterpret_cast<float4*>(P.comb_out + static_cast<size_t>(row) * 16)[j] =
                   make_float4(crow[0], crow[1], crow[2], crow[3]);
               if (P.mixes_out != nullptr) {
-                float4* mo = reinterpret_cast<float4*>(P.mixes_out + static_cast<size_t>(token2) * 24);
+                float4* mo = reinterpret_cast<float4*>(P.mixes_out + static_cast<size_t>(row) * 24);
                 mo[2 + j] = make_float4(mrow[0], mrow[1], mrow[2], mrow[3]);
                 if (j == 0) mo[0] = make_float4(m0[0], m0[1], m0[2], m0[3]);
                 if (j == 1) mo[1] = make_float4(m1[0], m1[1], m1[2], m1[3]);
@@ -1031,6 +1099,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const bool two = rk + L < split;
             const float4* r0 = reinterpret_cast<const float4*>(gpart(pb, rk) + tl2 * PART_STRIDE);
             const float4* r1 = reinterpret_cast<const float4*>(gpart(pb, two ? rk + L : rk) + tl2 * PART_STRIDE);
+            if (!checked(in_gpart(P, reinterpret_cast<const float*>(r0), PART_STRIDE) &&
+                             in_gpart(P, reinterpret_cast<const float*>(r1), PART_STRIDE), P.status))
+              continue;
             float4 v0[NV], v1[NV];
 #pragma unroll
             for (int e = 0; e < NV; ++e) {
@@ -1069,13 +1140,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             crow[k] = jr == 0 ? cv[k] : jr == 1 ? cv[4 + k] : jr == 2 ? cv[8 + k] : cv[12 + k];
             mrow[k] = jr == 0 ? m[8 + k] : jr == 1 ? m[12 + k] : jr == 2 ? m[16 + k] : m[20 + k];
           }
-          if (in_range && lr < 4 && token2 < P.N) {
-            P.pre_out[static_cast<size_t>(token2) * 4 + jr] = pj;
-            P.post_out[static_cast<size_t>(token2) * 4 + jr] = uj;
-            reinterpret_cast<float4*>(P.comb_out + static_cast<size_t>(token2) * 16)[jr] =
+          const int row = token2 + planted_rows(P, blockIdx.x == 0 && it == 0 && base_t == 0 && lq == 0);
+          if (in_range && lr < 4 && token2 < P.N && checked(row >= 0 && row < P.N, P.status)) {
+            P.pre_out[static_cast<size_t>(row) * 4 + jr] = pj;
+            P.post_out[static_cast<size_t>(row) * 4 + jr] = uj;
+            reinterpret_cast<float4*>(P.comb_out + static_cast<size_t>(row) * 16)[jr] =
                 make_float4(crow[0], crow[1], crow[2], crow[3]);
             if (P.mixes_out != nullptr) {
-              float4* mo = reinterpret_cast<float4*>(P.mixes_out + static_cast<size_t>(token2) * 24);
+              float4* mo = reinterpret_cast<float4*>(P.mixes_out + static_cast<size_t>(row) * 24);
               mo[2 + jr] = make_float4(mrow[0], mrow[1], mrow[2], mrow[3]);
               if (jr == 0) mo[0] = make_float4(m[0], m[1], m[2], m[3]);
               if (jr == 1) mo[1] = make_float4(m[4], m[5], m[6], m[7]);
@@ -1298,6 +1370,7 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   const size_t counter_bytes = (static_cast<size_t>(ngroups) * 32 + 255) / 256 * 256;
   P.counters = reinterpret_cast<unsigned*>(scratch);
   P.gpart = reinterpret_cast<float*>(scratch + counter_bytes);
+  P.gpart_end = P.gpart + static_cast<size_t>(ngroups) * split * 2 * (PART_BYTES / 4);
   if (counter_bytes + static_cast<size_t>(ngroups) * split * 2 * PART_BYTES > a.scratch_bytes)
     return cudaErrorInvalidValue;
   P.N = static_cast<int>(a.N);

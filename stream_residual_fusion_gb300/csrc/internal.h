@@ -13,6 +13,15 @@ unsigned* status_word();
 unsigned long long* trace_buffer(int64_t ctas);
 
 constexpr unsigned STATUS_TIMEOUT = 1u;
+// Set by the bounds-checked build (MHC_CHECKED=1) when an index test fails; the access is skipped.
+constexpr unsigned STATUS_BOUNDS = 2u;
+// Flag bit of the checked build only: plant one out-of-range row index in a finisher store and
+// in an MXFP8 scale store, to show that the checks catch it (MHC_ERR_SHAPE elsewhere).
+constexpr unsigned FLAG_PLANT_OOB = 0x4u;
+
+#ifndef MHC_CHECKED
+#define MHC_CHECKED 0
+#endif
 
 struct StepArgs {
   const void* X;

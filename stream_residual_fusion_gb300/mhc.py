@@ -28,9 +28,11 @@ MHC_ERR_ALIAS = -4
 MHC_ERR_CUDA = -5
 MHC_ERR_TIMEOUT = -6
 MHC_ERR_WORKSPACE = -7
+MHC_ERR_BOUNDS = -8
 
 COMB_ROW_DEST = 0x1
 DEBUG_NEVER_ARRIVE = 0x2
+DEBUG_PLANT_OOB = 0x4          # bounds-checked build only
 SPLIT_SHIFT = 8
 TILE_SHIFT = 16
 
@@ -77,6 +79,7 @@ SIGNATURES = {
     "mhc_step_config": (_I, [_I64, _I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(_I)]),
     "mhc_version": (_I, []),
+    "mhc_checked_build": (_I, []),
 }
 
 
@@ -407,5 +410,6 @@ def set_trace(buffer=None):
 
 
 def get_status(stream=None) -> int:
-    """Synchronise the stream; MHC_OK or MHC_ERR_TIMEOUT (then cleared)."""
+    """Synchronise the stream; MHC_OK, MHC_ERR_BOUNDS (checked build) or MHC_ERR_TIMEOUT (then
+    cleared)."""
     return int(lib.mhc_get_status(_stream(stream)))

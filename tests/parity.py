@@ -13,6 +13,8 @@ Tolerances (stated once, used by every GPU test):
     that close to a boundary between E4M3 values); there the kernel's result must be one of the
     two decisions within reach.
 """
+from fractions import Fraction
+
 import numpy as np
 
 import oracle as O
@@ -108,3 +110,21 @@ def check_mxfp8(codes, scale, y_ref, ulps=Y_ULPS):
                              f"{i.tolist()}: got {got[tuple(i)]}, want {mx.e4m3_round(y_ref[tuple(i)] / X[tuple(i)])}")
     same = (scale == mx.mx_scale_code(np.abs(y_ref).reshape(N, -1, mx.MX_BLOCK).max(axis=2))).mean()
     assert same > 0.99, f"y_scale: only {same:.4f} of the blocks equal the oracle's"
+
+
+def near_tie_cases():
+    """(p, x) pairs, p float32 and x = 1 + m/128 a bf16 value, whose exact product A lies in
+    (1 + 2^-8, 1 + 2^-8 + 2^-24). Rounding A to float32 gives 1 + 2^-8; adding 2^-24 then lands on
+    a float32 tie that stays at 1 + 2^-8, a bf16 tie that goes to 1. A fused multiply-add
+    A + 2^-24 rounds to 1 + 2^-8 + 2^-23 instead, and that to the bf16 value 1 + 2^-7. Each
+    pair is checked with exact rationals."""
+    lo = Fraction(1) + Fraction(1, 2 ** 8)
+    out = []
+    for m in range(1, 128):
+        x1 = 1.0 + m / 128.0
+        c = np.float32(float((lo + Fraction(1, 2 ** 25)) / Fraction(x1)))
+        for p1 in (c, np.nextafter(c, np.float32(2)), np.nextafter(c, np.float32(0))):
+            if lo < Fraction(float(p1)) * Fraction(x1) < lo + Fraction(1, 2 ** 24):
+                out.append((float(p1), x1))
+                break
+    return out

@@ -5,7 +5,8 @@ import pytest
 import torch
 
 import oracle as O
-from tests.parity import TOL_PUC, assert_abs, assert_bf16_within, assert_exact, assert_mixes, to64
+from tests.parity import (TOL_PUC, assert_abs, assert_bf16_within, assert_exact, assert_mixes,
+                          near_tie_cases, oracle_step, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -119,3 +120,47 @@ def test_mixes(M, synth, N, d, split):
     assert_abs(to64(o["pre"]), p, TOL_PUC, "pre")
     assert_abs(to64(o["post"]), u, TOL_PUC, "post")
     assert_abs(to64(o["comb"]), C, TOL_PUC, "comb")
+
+
+def test_products_rounded_before_the_sum_on_gpu(M, synth):
+    """Constructed near ties (tests/parity.py near_tie_cases): per token, stream 2 of X' sums
+    2^-24 * X_0 (X_0 = 1) and p * X_1 (X_1 = x) through comb, stream 3 adds the sublayer term
+    p * F (F = x) to 2^-24 * X_0. Products rounded before the sum give exactly 1 in both; a fused
+    multiply-add would give 1 + 2^-7. hc_pre with pre = (2^-24, p, 0, 0) over X'_0 = 1,
+    X'_1 = x gives 1 the same way. Checked for the standalone hc_post / hc_pre kernels and for
+    X' of the fused step, and against the oracle."""
+    cases = near_tie_cases()
+    N, d = len(cases), 128
+    assert N > 10
+    p = torch.tensor([c[0] for c in cases], device=DEV)
+    x = torch.tensor([c[1] for c in cases], device=DEV)
+    inp = synth.make_inputs(N, 4, d, seed=61, device=DEV)
+    X = torch.randn(N, 4, d, device=DEV)
+    X[:, 0] = 1.0
+    X[:, 1] = x[:, None]
+    inp["X"] = X.to(torch.bfloat16)
+    inp["F"] = x[:, None].expand(N, d).to(torch.bfloat16).contiguous()
+    C = torch.zeros(N, 4, 4, device=DEV)
+    C[:, 0, 0] = 1.0                     # X'_0 = X_0 = 1
+    C[:, 1, 1] = 1.0                     # X'_1 = X_1 = x
+    C[:, 0, 2] = 2.0 ** -24
+    C[:, 1, 2] = p                       # X'_2 = 2^-24 * 1 + p * x
+    C[:, 0, 3] = 2.0 ** -24              # X'_3 = p * F + 2^-24 * 1
+    u = torch.zeros(N, 4, device=DEV)
+    u[:, 3] = p
+    pre = torch.zeros(N, 4, device=DEV)
+    pre[:, 0] = 2.0 ** -24
+    pre[:, 1] = p
+    inp.update(comb=C, post=u, pre=pre)
+    Xp = M.hc_post(inp["X"], inp["F"], u, C)
+    assert torch.equal(Xp[:, 0], inp["X"][:, 0]) and torch.equal(Xp[:, 1], inp["X"][:, 1])
+    assert bool((Xp[:, 2:] == 1.0).all()), "hc_post: a product was fused into its sum"
+    yh = M.hc_pre(Xp, pre)
+    assert bool((yh == 1.0).all()), "hc_pre: a product was fused into its sum"
+    out = M.fused_step(inp["X"], inp["F"], pre, u, C, inp["W"], inp["scale"], inp["base"],
+                       inp["gain"], with_mixes=True)
+    assert M.get_status() == M.MHC_OK
+    assert torch.equal(out["Xp"], Xp)
+    ref = oracle_step(inp)
+    assert_exact(to64(Xp), ref["Xp"], "X'")
+    assert_exact(to64(yh), ref["y_hat"], "y_hat")

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle as O
+from tests.parity import near_tie_cases
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -137,16 +138,9 @@ def test_hc_products_rounded_before_the_sum():
     first gives 1 + 2^-8, plus 2^-24 is a float32 tie that stays there, a bf16 tie that goes to
     even: 1. A fused multiply-add would keep A's low bits and give 1 + 2^-7."""
     cases = 0
-    for m in range(1, 128):
-        x1 = 1.0 + m / 128.0                                   # a bf16 value
-        lo = Fraction(1) + Fraction(1, 2 ** 8)
-        c = np.float32(float((lo + Fraction(1, 2 ** 25)) / Fraction(x1)))
-        for p1 in (c, np.nextafter(c, np.float32(2)), np.nextafter(c, np.float32(0))):
-            A = Fraction(float(p1)) * Fraction(x1)
-            if lo < A < lo + Fraction(1, 2 ** 24):
-                break
-        else:
-            continue
+    for p1, x1 in near_tie_cases():
+        A = Fraction(float(p1)) * Fraction(x1)
+        p1 = np.float32(p1)
         Xp = np.zeros((1, 4, 1))
         Xp[0, 0, 0], Xp[0, 1, 0] = 1.0, x1
         pre = np.array([[2.0 ** -24, float(p1), 0.0, 0.0]])
