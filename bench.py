@@ -7,8 +7,10 @@ their three bf16 planes (mhc_pack_weights) and the fused kernel (mhc_fused_step_
 X and F once and writes X', y, p, u, C. The workload is the prefill batch B=4, T=8192
 (N = 32,768 tokens, 3.4 GB of streams per step, far larger than L2), seeded synthetic inputs.
 
-Tokens are independent, so N GPUs run N independent batches (weak scaling, no collective on the
-data path); the printed value is all ranks' tokens over the slowest rank's time.
+Tokens are independent, so N GPUs run N independent batches (weak scaling, the default; no
+collective on the data path); the printed value is all ranks' tokens over the slowest rank's time.
+--scaling strong splits one batch into contiguous token shards, one per rank, and reports the
+batch's tokens over the slowest rank's time.
 
 --impl reference times the CPU oracle (the only reference this method has) on a bounded sample
 of the same workload on the host cores.
@@ -156,12 +158,14 @@ class ClockSampler:
 
 
 def _oracle_chunk(args):
-    seed, lo, hi = args
+    seed, lo, hi = args[:3]
+    workload = args[3] if len(args) > 3 else WORKLOAD
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     import oracle as O
     from stream_residual_fusion_gb300 import synth
-    w = synth.WORKLOADS[WORKLOAD]
-    inp = synth.make_inputs(hi - lo, 4, w.d, seed=seed, scale_uniform=w.scale_uniform)
+    w = synth.WORKLOADS[workload]
+    inp = synth.make_inputs(hi - lo, 4, w.d, seed=seed, scale_uniform=w.scale_uniform,
+                            x_stream_std=w.x_stream_std, outlier_frac=w.outlier_frac)
     a = O.inputs_to_f64(inp)
     t0 = time.perf_counter()
     O.fused_step(a["X"], a["F"], a["pre"], a["post"], a["comb"], a["W"], a["scale"], a["base"],
@@ -197,6 +201,97 @@ def oracle_throughput(tokens_per_worker: int = 256):
               f"single-threaded processes x {tokens_per_worker} tokens; slowest worker {busy:.1f} s "
               f"(wall {wall:.1f} s incl. start-up)")
     return toks / busy, cores, sample
+
+
+def oracle_rate(workload: str, tokens: int, workers: int, chunk: int = 2048):
+    """Tokens/s of the oracle on `tokens` tokens of `workload`, cut into chunks of at most
+    `chunk` tokens spread over `workers` spawned single-threaded processes; the time is the
+    slowest worker's busy time (start-up excluded)."""
+    import multiprocessing as mp
+    env_keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    os.environ.update({k: "1" for k in env_keys})
+    try:
+        per = -(-tokens // workers)
+        jobs = []
+        for w_ in range(workers):
+            n = min(per, tokens - w_ * per)
+            if n > 0:
+                jobs.append([(8000 + w_ * 97 + c, 0, min(chunk, n - c), workload)
+                             for c in range(0, n, chunk)])
+        with mp.get_context("spawn").Pool(len(jobs)) as pool:
+            res = pool.map(_oracle_jobs, jobs)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return sum(r[0] for r in res) / max(r[1] for r in res)
+
+
+def _oracle_jobs(jobs):
+    toks = busy = 0.0
+    for j in jobs:
+        t, b = _oracle_chunk(j)
+        toks += t
+        busy += b
+    return toks, busy
+
+
+def run_table(args):
+    """Per workload: the oracle on all host cores and on one core (median of 3 runs after one
+    warm-up, a bounded sample of tokens), and the fused kernel's p50 on the GPU (>= 100 launches,
+    >= 20 for the largest; L2 flushed between launches where the streams fit in it). One JSON
+    line per workload."""
+    import torch
+    from stream_residual_fusion_gb300 import mhc, synth
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    for name, w in synth.WORKLOADS.items():
+        row = {"workload": name, "config": w.name, "N": w.N, "cores": cores}
+        for label, workers, cap in (("all_cores", cores, args.table_tokens),
+                                    ("one_core", 1, max(8, args.table_tokens // 8))):
+            n = min(w.N, cap)
+            oracle_rate(name, min(n, 8), 1)                       # warm-up
+            rates = [oracle_rate(name, n, workers) for _ in range(3)]
+            row[f"oracle_{label}_tok_s"] = statistics.median(rates)
+            row[f"oracle_{label}_sample_tokens"] = n
+        if dev is not None:
+            inp = synth.make_workload(w, seed=3000, device=dev)
+            inp.pop("outliers", None)
+            Wp = mhc.pack_weights(inp["W"])
+            scratch = torch.empty(mhc.step_scratch_bytes(w.d), dtype=torch.uint8, device=dev)
+            out = mhc.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None,
+                                 inp["scale"], inp["base"], inp["gain"], W_packed=Wp,
+                                 scratch=scratch)
+            flush = (torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+                     if w.N * STREAM_BYTES_PER_TOKEN < 2 * L2_BYTES else None)
+            reps = 20 if w.N >= 100000 else 100
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps + 10)]
+            for i, (a, b) in enumerate(ev):
+                if flush is not None:
+                    flush.fill_(1)
+                a.record()
+                mhc.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None,
+                               inp["scale"], inp["base"], inp["gain"], W_packed=Wp,
+                               scratch=scratch, out=out)
+                b.record()
+            torch.cuda.synchronize()
+            ms = sorted(a.elapsed_time(b) for a, b in ev[10:])
+            row.update(gpu_launches=reps, gpu_p50_ms=percentile(ms, 50), gpu_p95_ms=percentile(ms, 95),
+                       gpu_p99_ms=percentile(ms, 99),
+                       gpu_tok_s=w.N / (percentile(ms, 50) / 1e3),
+                       frac_measured=algorithmic_bytes(w.N, w.d) / (percentile(ms, 50) / 1e3) / 1e9 / peak,
+                       frac_nominal=algorithmic_bytes(w.N, w.d) / (percentile(ms, 50) / 1e3) / 1e9 / 8000.0,
+                       peak_kind=peak_kind, l2=("flushed" if flush is not None else "inputs > L2"))
+            del inp, out, Wp, scratch, flush
+            torch.cuda.empty_cache()
+        print(json.dumps(row), flush=True)
+    return 0
 
 
 def run_reference(args):
@@ -251,12 +346,20 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     from stream_residual_fusion_gb300 import mhc, synth
-    from stream_residual_fusion_gb300.dist import max_over_ranks, weak_scaling_throughput
+    from stream_residual_fusion_gb300.dist import (max_over_ranks, slice_tokens,
+                                                   strong_scaling_throughput, token_shard,
+                                                   weak_scaling_throughput)
     w = synth.WORKLOADS[WORKLOAD]
-    N, d = w.N, w.d
-    inp = synth.make_workload(w, seed=3000 + rank, device=dev)
-    if "outliers" in inp:
-        del inp["outliers"]
+    N_total, d = w.N, w.d
+    strong = args.scaling == "strong"
+    # weak: every rank steps its own batch of the workload; strong: one batch, each rank its
+    # contiguous token shard (the same batch on every rank: one seed)
+    inp = synth.make_workload(w, seed=3000 if strong else 3000 + rank, device=dev)
+    inp.pop("outliers", None)
+    if strong:
+        lo, hi = token_shard(N_total, rank, world)
+        inp.update({k: v.clone() for k, v in slice_tokens(inp, lo, hi).items()})
+    N = inp["X"].shape[0]                    # tokens this rank steps
     torch.cuda.synchronize()
 
     out = {"Xp": torch.empty_like(inp["X"]), "y": torch.empty(N, d, dtype=torch.bfloat16, device=dev),
@@ -353,7 +456,11 @@ def run_ours(args):
 
     total_ms = max_over_ranks(total_ms, device=dev)          # the slowest rank's time
     ms_per_step = total_ms / K
-    value = weak_scaling_throughput(N, world, ms_per_step / 1e3)
+
+    def throughput(seconds):
+        return (strong_scaling_throughput(N_total, seconds) if strong
+                else weak_scaling_throughput(N, world, seconds))
+    value = throughput(ms_per_step / 1e3)
 
     # ------------------------------------------------------------------ end to end, host buffers
     e2e = None
@@ -383,7 +490,7 @@ def run_ours(args):
         b.record(stream)
         torch.cuda.synchronize()
         te = max_over_ranks(a.elapsed_time(b) / e2e_steps, device=dev)
-        e2e = {"value": weak_scaling_throughput(N, world, te / 1e3), "unit": "tokens/s",
+        e2e = {"value": throughput(te / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": te, "steps": e2e_steps,
                "call": f"mhc_fused_step_host (pinned host tensors, {chunk}-token chunks)"}
@@ -402,8 +509,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name} (N={N}), n=4, d={d}", "B": w.B, "T": w.T, "n": 4, "d": d,
+        "scaling": args.scaling, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} (N={N_total}), n=4, d={d}", "B": w.B, "T": w.T, "n": 4, "d": d,
+                   "tokens_per_rank": N,
                    "sinkhorn_iters": 20, "comb_reading": "code: X'_k = u_k F + sum_j C_jk X_j",
                    "l2": (f"inputs larger than L2 ({N * 51200 / 1e9:.2f} GB of streams read per step)"
                           if N * 51200 > 129e6 else "inputs smaller than L2 (not flushed)"),
@@ -628,6 +736,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--table", action="store_true",
+                    help="per-workload table: the oracle on all host cores and on one core beside "
+                         "the fused kernel's GPU p50")
+    ap.add_argument("--table-tokens", type=int, default=2048,
+                    help="oracle sample per run for --table (one core: an eighth of it)")
+    ap.add_argument("--scaling", choices=("weak", "strong"), default="weak",
+                    help="weak: every rank steps a whole batch; strong: one batch split into "
+                         "contiguous token shards over the ranks")
     ap.add_argument("--pct-launches", type=int, default=200,
                     help="launches of the percentile pass after the timed region (>= 100)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -649,6 +765,8 @@ def main():
     args.pct_launches = max(100, args.pct_launches)
     if args.impl == "reference":
         return run_reference(args)
+    if args.table:
+        return run_table(args)
     if args.form == "unfused":
         return run_unfused(args)
     if args.form == "mxfp8":

@@ -164,6 +164,7 @@ struct StepParams {
   int iters;
   float hc_eps;
   float norm_eps;
+  float neg_zero;              // -0.0: the run-time zero addend of the rounded products (hc_arith.cuh)
   unsigned flags;
 };
 
@@ -609,6 +610,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto slot_addr = [&](int slot) { return stash + static_cast<uint32_t>(slot * PASS_COLS); };
 
     f2 cu[4], cc[4][4], cp[4];
+    const f2 nz2{P.neg_zero, P.neg_zero};
     // this token's coefficients of tile iteration it_, from the tile's sums buffer (copied in by
     // the poster lane)
     auto load_coeffs = [&](int it_, int tile) {
@@ -768,11 +770,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int k = 0; k < 4; ++k) {
                   // X'_k: rounded products summed in stream order (hc_arith.cuh)
                   const f2 ck[4] = {cc[0][k], cc[1][k], cc[2][k], cc[3][k]};
-                  ow[k][w] = f2_to_bf2(hc_post_pair(ck, cu[k], x, f));
+                  ow[k][w] = f2_to_bf2(hc_post_pair(ck, cu[k], x, f, nz2));
                   xp[k] = bf2_to_f2(ow[k][w]);
                   lx = fma2(xp[k], xp[k], lx);
                 }
-                ywall[4 * q + w] = f2_to_bf2(hc_pre_pair(cp, xp));
+                ywall[4 * q + w] = f2_to_bf2(hc_pre_pair(cp, xp, nz2));
                 const f2 yr = bf2_to_f2(ywall[4 * q + w]);
                 ly = fma2(yr, yr, ly);
               }
@@ -1382,6 +1384,7 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   P.iters = a.iters;
   P.hc_eps = a.hc_eps;
   P.norm_eps = a.norm_eps;
+  P.neg_zero = -0.0f;
   P.flags = a.flags;
 
   e = cudaMemsetAsync(P.counters, 0, static_cast<size_t>(ngroups) * 32, stream);

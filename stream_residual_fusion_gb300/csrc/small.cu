@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_row_kernel(const uint4* _
 // hc_arith.cuh, as in the fused kernel).
 __global__ void hc_post_kernel(const uint4* __restrict__ X, const uint4* __restrict__ F,
                                const float* __restrict__ post, const float* __restrict__ comb,
-                               uint4* __restrict__ Xo, int64_t N, int d, int row_dest) {
+                               uint4* __restrict__ Xo, int64_t N, int d, int row_dest,
+                               float neg_zero) {
   const int chunks = d / 8;
   const int64_t total = N * chunks;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -212,7 +213,7 @@ __global__ void hc_post_kernel(const uint4* __restrict__ X, const uint4* __restr
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const f2 ck[4] = {cc[0][k], cc[1][k], cc[2][k], cc[3][k]};
-        ow[k][w] = f2_to_bf2(hc_post_pair(ck, cu[k], x, f));
+        ow[k][w] = f2_to_bf2(hc_post_pair(ck, cu[k], x, f, f2{neg_zero, neg_zero}));
       }
     }
 #pragma unroll
@@ -222,7 +223,7 @@ __global__ void hc_post_kernel(const uint4* __restrict__ X, const uint4* __restr
 
 // hc_pre alone: y_hat = bf16 of the float32 evaluation of hc_arith.cuh.
 __global__ void hc_pre_kernel(const uint4* __restrict__ Xp, const float* __restrict__ pre,
-                              uint4* __restrict__ y, int64_t N, int d) {
+                              uint4* __restrict__ y, int64_t N, int d, float neg_zero) {
   const int chunks = d / 8;
   const int64_t total = N * chunks;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -246,7 +247,7 @@ __global__ void hc_pre_kernel(const uint4* __restrict__ Xp, const float* __restr
         const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
         x[j] = bf2_to_f2(xw[w]);
       }
-      o[w] = f2_to_bf2(hc_pre_pair(cp, x));
+      o[w] = f2_to_bf2(hc_pre_pair(cp, x, f2{neg_zero, neg_zero}));
     }
     y[t * chunks + c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
@@ -299,7 +300,7 @@ cudaError_t launch_hc_post(const void* X, const void* F, const float* post, cons
   const int threads = 256;
   hc_post_kernel<<<grid_for(N * (d / 8), threads), threads, 0, stream>>>(
       static_cast<const uint4*>(X), static_cast<const uint4*>(F), post, comb,
-      static_cast<uint4*>(X_out), N, d, row_dest ? 1 : 0);
+      static_cast<uint4*>(X_out), N, d, row_dest ? 1 : 0, -0.0f);
   return cudaGetLastError();
 }
 
@@ -307,7 +308,7 @@ cudaError_t launch_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t
                           cudaStream_t stream) {
   const int threads = 256;
   hc_pre_kernel<<<grid_for(N * (d / 8), threads), threads, 0, stream>>>(
-      static_cast<const uint4*>(Xp), pre, static_cast<uint4*>(y_hat), N, d);
+      static_cast<const uint4*>(Xp), pre, static_cast<uint4*>(y_hat), N, d, -0.0f);
   return cudaGetLastError();
 }
 

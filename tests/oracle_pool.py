@@ -74,10 +74,12 @@ def check_chunk(task):
 
 
 def full_parity(inp: dict, out: dict, *, chunk: int = 512, workers: int | None = None,
-                oracle_kw: dict | None = None) -> int:
+                oracle_kw: dict | None = None, timeout_s: float = 900.0) -> int:
     """Compare every token of `out` (the GPU step's outputs, CUDA tensors; y as bf16 `y`, or as
-    MXFP8 `y_codes` and `y_scale`) with the oracle on `inp` (the step's inputs). Raises AssertionError naming the first failing chunk; returns the
-    number of tokens compared."""
+    MXFP8 `y_codes` and `y_scale`) with the oracle on `inp` (the step's inputs). Raises
+    AssertionError naming the first failing chunk; returns the number of tokens compared. A pool
+    that does not finish within `timeout_s` (a worker that died at start-up, for example) fails
+    the comparison instead of waiting forever."""
     import multiprocessing as mp
     N = inp["X"].shape[0]
     if workers is None:
@@ -113,17 +115,22 @@ def full_parity(inp: dict, out: dict, *, chunk: int = 512, workers: int | None =
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = v
+    import time
+    deadline = time.monotonic() + timeout_s
     with pool:
         pending = []
         for lo in range(0, N, chunk):
             hi = min(N, lo + chunk)
-            gate.acquire()
+            if not gate.acquire(timeout=max(1.0, deadline - time.monotonic())):
+                raise AssertionError(f"oracle pool made no progress within {timeout_s:.0f} s")
             ins = {k: _to_host(inp[k][lo:hi]) for k in PER_TOKEN_IN}
             outs = {k: _to_host(out[k][lo:hi]) for k in outs_keys}
             pending.append(pool.apply_async(check_chunk, ((lo, hi, ins, outs, oracle_kw or {}),),
                                             callback=done, error_callback=fail))
         for r in pending:
-            r.wait()
+            r.wait(max(1.0, deadline - time.monotonic()))
+            if not r.ready():
+                raise AssertionError(f"oracle pool did not finish within {timeout_s:.0f} s")
     if failures:
         failures.sort()
         raise AssertionError(f"{len(failures)} chunk(s) failed; first: {failures[0][1]}")

@@ -113,3 +113,29 @@ def test_host_pipeline_repeated_calls_reuse_staging(M, synth):
         M.fused_step_host(h["X"], h["F"], h["pre"], h["post"], h["comb"], inp["W"], inp["scale"],
                           inp["base"], inp["gain"], chunk_tokens=256, staging=stg)
     np.testing.assert_equal(M.get_status(), M.MHC_OK)
+
+
+def test_sharded_step_over_device_replicas(M, synth):
+    """dist.fused_step_sharded: one host batch cut into contiguous token shards, each run by the
+    host-tensor step on its replica's device and written into its rows of the host outputs. With
+    one GPU every replica sits on cuda:0 (three shards, uneven), which runs the same dispatch;
+    the result equals the unsharded host-tensor step bit for bit. (The launch shape is pinned:
+    a token's sums are grouped by the CTAs of its tile, so an automatic shape that differs with
+    the launch's token count may move the mix numbers in their last bits.)"""
+    from stream_residual_fusion_gb300 import dist
+    N, d = 1001, 5120
+    inp = synth.make_inputs(N, 4, d, seed=4242, scale_uniform=True)
+    host = {k: inp[k].pin_memory() for k in ("X", "F", "pre", "post", "comb")}
+    par = {k: inp[k].to(DEV) for k in ("W", "scale", "base", "gain")}
+    reps = dist.replicate_params(par["W"], par["scale"], par["base"], par["gain"],
+                                 [DEV] * 3, chunk_tokens=256, with_mixes=True)
+    flags = M.split_flag(8) | M.tile_flag(32)
+    got = dist.fused_step_sharded(host["X"], host["F"], host["pre"], host["post"], host["comb"],
+                                  reps, with_mixes=True, flags=flags)
+    want = M.fused_step_host(host["X"], host["F"], host["pre"], host["post"], host["comb"],
+                             par["W"], par["scale"], par["base"], par["gain"], with_mixes=True,
+                             chunk_tokens=256, flags=flags)
+    torch.cuda.synchronize()
+    assert M.get_status() == M.MHC_OK
+    for k in want:
+        assert torch.equal(got[k], want[k]), k
