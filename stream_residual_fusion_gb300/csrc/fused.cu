@@ -84,7 +84,8 @@ static_assert(4 * HALVES * KSTEPS * PG == 16, "accumulation groups of 16 MMAs");
 constexpr int TILE_BYTES = TT * ROWB;               // one [TT tokens x DC] tile
 constexpr int STAGE_BYTES = 5 * TILE_BYTES;         // X_0..X_3 and F
 constexpr int RUN_STRIDE = 24;                      // floats per token of the local running sums
-// exchange row per token: 24 mix sums, then S_x of each of the TPT parts, then their S_y
+// exchange row per token: 24 mix sums, then S_x of each of the TPT parts (the rest of the row,
+// up to a whole float4, is unused). S_y goes through tagged words (below).
 constexpr int PART_STRIDE = 24 + 2 * TPT;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COLS = STEP_MMA_N;         // two accumulators, at columns 0 and 80
@@ -109,13 +110,15 @@ static_assert(COEF_COMB + TT * 64 <= RUN_BYTES, "coefficients fit a running-sum 
 constexpr int OFF_W = NSTAGE * STAGE_BYTES;
 constexpr int OFF_PART = OFF_W + NW * STEP_WBLOCK_BYTES;
 constexpr int OFF_BARS = OFF_PART + 2 * RUN_BYTES;
-// full/empty/xready per X/F slot; wfull/wempty per weight entry; accready[2]; posted[2];
-// mposted[2]; pfreed[2]; sygrp[2]; cfull[2]; drained; never
-constexpr int NBARS = 3 * NSTAGE + 2 * NW + 14;
+// full/empty/xready per X/F slot; wfull/wempty per weight entry; accready[2]; mposted[2];
+// pfreed[2]; cfull[2]; drained; never
+constexpr int NBARS = 3 * NSTAGE + 2 * NW + 10;
 constexpr int OFF_TMEM = OFF_BARS + NBARS * 8;
 // MXFP8 y: each thread's block-maximum exponent for its partner, [2 slot parities][2 parts][TT]
 constexpr int OFF_XCH = OFF_TMEM + 16;
-constexpr int SMEM_BYTES = OFF_XCH + 4 * TT + 1024;   // + slack for 1 KB alignment
+// a tile's S_y of each of a token's TPT parts, summed per token before it is posted, [TPT][TT]
+constexpr int OFF_SYX = OFF_XCH + 4 * TT;
+constexpr int SMEM_BYTES = OFF_SYX + 4 * TPT * TT + 1024;   // + slack for 1 KB alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(STAGE_BYTES % 1024 == 0 && STEP_WBLOCK_BYTES % 1024 == 0, "tile alignment");
 
@@ -152,7 +155,11 @@ struct StepParams {
   uint8_t* y_scale;            // MXFP8 y only: E8M0 block scales [N, d / 32]
   unsigned* status;
   unsigned long long* trace;   // optional: 8 phase timestamps per (tile, CTA) (mhc_set_trace)
-  unsigned* counters;          // per group: syready[2], pready[2], pfree[2] (zeroed per launch)
+  unsigned* counters;          // per group: pready[2] at 2, pfree[2] at 4 (zeroed per launch)
+  // per group: [2 buffers][TT tokens][split ranks] tagged words {S_y of the token over the
+  // rank's columns, tile iteration + 1} (zeroed per launch)
+  unsigned long long* sytag;
+  const unsigned long long* sytag_end;
   float* gpart;                // per group: [2 buffers][split ranks][TT tokens][PART_STRIDE]
   const float* gpart_end;      // end of the exchange area (bounds of the checked build)
   int N;
@@ -332,11 +339,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* wfull = xready + NSTAGE;        // [NW]: the block in weight entry e has landed
   uint64_t* wempty = wfull + NW;            // [NW]: the MMAs that read weight entry e are done
   uint64_t* accready = wempty + NW;         // [2]: an accumulation group finished in buffer i
-  uint64_t* posted = accready + 2;          // [2]: the consumer warps wrote a tile's S_x, S_y
-  uint64_t* mposted = posted + 2;           // [2]: the folding warps wrote a tile's mix sums
+  uint64_t* mposted = accready + 2;         // [2]: the folding warps wrote a tile's mix sums
   uint64_t* pfreed = mposted + 2;           // [2]: the group's finishers released an exchange buffer
-  uint64_t* sygrp = pfreed + 2;             // [2]: every rank of the group posted a tile's S_y
-  uint64_t* cfull = sygrp + 2;              // [2]: a tile's coefficients are in its sums buffer
+  uint64_t* cfull = pfreed + 2;             // [2]: a tile's coefficients are in its sums buffer
   uint64_t* drained = cfull + 2;            // the last X'/y stores have left the ring
   uint64_t* never = drained + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
@@ -350,11 +355,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int nclust = gridDim.x / split;               // groups
   const int c0 = blockIdx.x / split;                  // this CTA's group = its first tile
   // group exchange (global memory): counters and the partial sums of every rank
-  unsigned* const syready = P.counters + 8 * c0;      // [2]: consumer warps that posted S_x, S_y
-  unsigned* const pready = syready + 2;               // [2]: consumer warps that posted mix sums
-  unsigned* const pfree = syready + 4;                // [2]: finishers done reading a buffer
+  unsigned* const pready = P.counters + 8 * c0 + 2;   // [2]: consumer warps that posted mix sums
+  unsigned* const pfree = pready + 2;                 // [2]: finishers done reading a buffer
   auto gpart = [&](int pb, int rank) {
     return P.gpart + ((static_cast<size_t>(c0) * 2 + pb) * split + rank) * (TT * PART_STRIDE);
+  };
+  // the tagged S_y words of token row tl, rank 0 (the ranks follow)
+  auto sytag = [&](int pb, int tl_) {
+    return P.sytag + ((static_cast<size_t>(c0) * 2 + pb) * TT + tl_) * split;
   };
   const int col0 = static_cast<int>(g) * DC;          // first column of this CTA's slice
   const int cstride = DC * split;                     // stride between its slots' columns
@@ -386,10 +394,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&accready[0], 1);
     mbar_init(&accready[1], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&posted[i], NCONS);
       mbar_init(&mposted[i], NFOLD);
       mbar_init(&pfreed[i], 1);
-      mbar_init(&sygrp[i], 1);
       mbar_init(&cfull[i], 1);
     }
     mbar_init(drained, 1);
@@ -445,11 +451,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // memory load. Per tile, in order:
       //   1. (from the third tile) wait until the group's finishers have released exchange
       //      buffer it & 1, then tell the consumers (pfreed);
-      //   2. once the consumer warps wrote their S_x, S_y (posted), add their count to the
-      //      group's syready counter with one release;
-      //   3. wait until every rank has done so, then tell the consumers (sygrp): the tile's RMS
-      //      factors can be read;
-      //   4. once the folding warps wrote the tile's mix sums (mposted), release pready.
+      //   2. once the folding warps wrote the tile's mix sums and S_x (mposted; every consumer
+      //      warp folds), release pready.
+      // (The tile's S_y goes to the group through tagged words the consumers post and poll
+      // themselves.)
       // Causality runs through this lane: the peers' release, its acquire, its CTA-scope
       // arrive, the consumers' wait.
       // It also copies each tile's coefficients into the tile's running-sum buffer, one and a
@@ -480,13 +485,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!gwait(&pfree[it & 1], static_cast<unsigned>((it >> 1) * split), limit()))
             timed_out = true;
           mbar_arrive(&pfreed[it & 1]);
-        }
-        if (FUSED) {
-          if (!mbar_wait(&posted[it & 1], (it >> 1) & 1, limit())) timed_out = true;
-          gcount_release_n(&syready[it & 1], NCONS);
-          if (!gwait(&syready[it & 1], static_cast<unsigned>(((it >> 1) + 1) * split * NCONS), limit()))
-            timed_out = true;
-          mbar_arrive(&sygrp[it & 1]);
         }
         if (!mbar_wait(&mposted[it & 1], (it >> 1) & 1, limit())) timed_out = true;
         gcount_release_n(&pready[it & 1], NFOLD);
@@ -638,39 +636,59 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto part_of = [&](int it_) {   // running sums of this thread for tile iteration it_
       return reinterpret_cast<float*>(sm + OFF_PART + (it_ & 1) * RUN_BYTES) + tl * RUN_STRIDE;
     };
-    // RMS factor of tile iteration it_ for this token: y_hat sums of squares of every slice
-    // RMS factor of tile iteration it_ for this token: y_hat sums of squares of every slice. In
-    // two halves, so the L2 latency overlaps other work: rms_issue waits for the group's count
-    // and issues the loads of the last eight ranks (earlier ranks, if any, are summed at once);
-    // rms_finish adds them up.
-    float rms_sy = 0.f, rms_v[8];
-    auto rms_issue = [&](int it_) {
-      // every rank posted tile it_'s S_y (seen by the poster lane)
-      if (!mbar_wait(&sygrp[it_ & 1], (it_ >> 1) & 1, limit())) timed_out = true;
-      rms_sy = 0.f;
-      for (int rk0 = 0; rk0 < split; rk0 += 8) {
-        if (rk0 > 0) rms_sy += ((rms_v[0] + rms_v[1]) + (rms_v[2] + rms_v[3])) +
-                               ((rms_v[4] + rms_v[5]) + (rms_v[6] + rms_v[7]));
+    // RMS factor of tile iteration it_ for this token, from the group's tagged S_y words (one per
+    // rank, tag it_ + 1). In two halves, so that the L2 round trip overlaps other work:
+    // rms_issue loads the words of the last eight ranks (earlier ranks, if any, are summed at
+    // once); rms_finish polls again any word whose tag was not there yet and adds them up, in
+    // rank order. Rows at and past the tile height have no words and take no factor.
+    float rms_sy = 0.f;
+    uint64_t rms_w[8];
+    auto rms_sum8 = [&](int it_, int rk0) {   // the words of ranks rk0.., polled until complete
+      const uint32_t want = static_cast<uint32_t>(it_) + 1u;
+      const unsigned long long* row = sytag(it_ & 1, tl) + rk0;
+      float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          rms_v[u] = 0.f;
-          if (rk0 + u < split) {
-            const float* row = gpart(it_ & 1, rk0 + u) + tl * PART_STRIDE + 24 + TPT;
-            if (!checked(in_gpart(P, row, TPT), P.status)) continue;
-            if constexpr (TPT == 4) {
-              const float4 q4 = __ldcg(reinterpret_cast<const float4*>(row));
-              rms_v[u] = (q4.x + q4.y) + (q4.z + q4.w);
-            } else {
-              const float2 q2 = __ldcg(reinterpret_cast<const float2*>(row));
-              rms_v[u] = q2.x + q2.y;
-            }
+      for (int u = 0; u < 8; ++u) {
+        v[u] = 0.f;
+        if (rk0 + u < split && tl < tt && (!MHC_CHECKED || (row + u >= P.sytag && row + u < P.sytag_end))) {
+          uint64_t w = rms_w[u];
+          if (word_tag(w) != want) {
+            const uint64_t t0 = global_timer_ns();
+            const uint64_t lim = limit();
+            do {
+              w = tagged_load(row + u);
+              if (word_tag(w) == want) break;
+              if (global_timer_ns() - t0 > lim) {
+                timed_out = true;
+                break;
+              }
+            } while (true);
           }
+          v[u] = word_value(w);
         }
       }
+      return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
     };
-    auto rms_finish = [&]() {
-      const float sy = rms_sy + (((rms_v[0] + rms_v[1]) + (rms_v[2] + rms_v[3])) +
-                                 ((rms_v[4] + rms_v[5]) + (rms_v[6] + rms_v[7])));
+    auto rms_load8 = [&](int it_, int rk0) {
+      const unsigned long long* row = sytag(it_ & 1, tl) + rk0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        rms_w[u] = 0;
+        if (rk0 + u < split && tl < tt && checked(row + u >= P.sytag && row + u < P.sytag_end, P.status))
+          rms_w[u] = tagged_load(row + u);
+      }
+    };
+    int rms_last = 0;                      // first rank of the words loaded by rms_issue
+    auto rms_issue = [&](int it_) {
+      rms_sy = 0.f;
+      for (int rk0 = 0; rk0 < split; rk0 += 8) {
+        if (rk0 > 0) rms_sy += rms_sum8(it_, rk0 - 8);
+        rms_load8(it_, rk0);
+        rms_last = rk0;
+      }
+    };
+    auto rms_finish = [&](int it_) {
+      const float sy = rms_sy + rms_sum8(it_, rms_last);
       const float r = __frsqrt_rn(__fdiv_rn(sy, static_cast<float>(d)) + P.norm_eps);
       return f2{r, r};
     };
@@ -786,7 +804,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             stash_store(slot_addr(slot), ywall);
           }
           // the previous tile's RMS factor: its loads were issued after slot RLAG - 1
-          if (s == RLAG && it > 0) r_new = rms_finish();
+          if (s == RLAG && it > 0) r_new = rms_finish(it - 1);
           if (consume) {
             // y of global slot gs - R into the F tile (read above)
             const f2 r_src = s >= RLAG ? r_new : r_old;
@@ -855,19 +873,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       take_coeffs(it + 1);
 
       // ------------------------------------------------------------ post this slice's sums
-      // row layout: [0..23] mix sums (folder half h owns 12h..12h+11), [24 + part] S_x,
-      // [24 + TPT + part] S_y.
+      // S_y: the token's two parts are added (part 0 + part 1, through shared memory between
+      // the two warps of this TMEM quarter) and posted as one tagged word, tag it + 1, which
+      // the group's consumers poll from slot RLAG - 1 of their next tile. Its buffer it & 1 is
+      // rewritten two tiles later, after every rank has read it: no rank gets past slot RLAG of
+      // tile it + 1 before all ranks posted tile it, which they do after reading tile it - 1.
+      if (FUSED) {
+        float* syx = reinterpret_cast<float*>(sm + OFF_SYX);
+        syx[part * TT + tl] = sy2.x + sy2.y;
+        named_bar_sync(3 + sub, 64);
+        if (part == 0 && tl < tt) {
+          unsigned long long* w = sytag(it & 1, tl) + g;
+          if (checked(w >= P.sytag && w < P.sytag_end, P.status))
+            tagged_store(w, syx[tl] + syx[TT + tl], static_cast<uint32_t>(it) + 1u);
+        }
+        named_bar_sync(3 + sub, 64);      // syx is free for the next tile
+      }
+      // exchange row layout: [0..23] mix sums (folder half h owns 12h..12h+11), [24 + part] S_x.
       // The group buffer it & 1 was last read (by every finisher) two tiles ago.
       if (it >= 2 && !mbar_wait(&pfreed[it & 1], ((it >> 1) - 1) & 1, limit())) timed_out = true;
       {
         float* pt = gpart(it & 1, g) + tl * PART_STRIDE;
-        if (checked(in_gpart(P, pt, PART_STRIDE), P.status)) {
-          pt[24 + part] = sx2.x + sx2.y;
-          pt[24 + TPT + part] = sy2.x + sy2.y;
-        }
+        if (checked(in_gpart(P, pt, PART_STRIDE), P.status)) pt[24 + part] = sx2.x + sx2.y;
       }
       __syncwarp();
-      if (FUSED && lane == 0) mbar_arrive(&posted[it & 1]);   // published by the poster (warp 0)
       if (tr && warp == NROLE && lane == 0) tr[6] = global_timer_ns() - tr[0];
     }
 
@@ -889,7 +918,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         gl[k] = i < S * DC ? __ldg(P.gain + col0 + (i / DC) * cstride + i % DC) : 0.f;
       }
       rms_issue(it - 1);
-      const f2 r_last = rms_finish();
+      const f2 r_last = rms_finish(it - 1);
       const f2 r_before = r_new;    // tile it-2's factor (computed during tile it-1)
 #pragma unroll
       for (int k = 0; k < GAIN_PER_THREAD; ++k) {
@@ -1316,9 +1345,9 @@ size_t step_scratch_bytes() {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 0;
-  // per CTA (at most one per SM): its group's counters (32 bytes, shared by the group) and two
-  // buffers of its partial sums
-  return 256 + static_cast<size_t>(sms) * (32 + 2 * PART_BYTES);
+  // per CTA (at most one per SM): its group's counters (32 bytes, shared by the group), two
+  // buffers of its tagged S_y words and two of its partial sums
+  return 256 + static_cast<size_t>(sms) * (32 + 2 * TT * 8 + 2 * PART_BYTES);
 }
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
@@ -1367,13 +1396,17 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   P.status = status_word();
   if (P.status == nullptr) return cudaErrorInvalidDevice;
   P.trace = trace_buffer(static_cast<int64_t>(split) * tiles);
-  // scratch: [256 B of group counters per 8 groups ... ] then the partial sums
+  // scratch: the group counters (32 B per group), the tagged S_y words (both zeroed by one
+  // memset per launch), then the partial sums
   uint8_t* scratch = static_cast<uint8_t*>(a.scratch);
   const size_t counter_bytes = (static_cast<size_t>(ngroups) * 32 + 255) / 256 * 256;
+  const size_t sytag_bytes = static_cast<size_t>(ngroups) * 2 * TT * split * 8;
   P.counters = reinterpret_cast<unsigned*>(scratch);
-  P.gpart = reinterpret_cast<float*>(scratch + counter_bytes);
+  P.sytag = reinterpret_cast<unsigned long long*>(scratch + counter_bytes);
+  P.sytag_end = P.sytag + sytag_bytes / 8;
+  P.gpart = reinterpret_cast<float*>(scratch + counter_bytes + sytag_bytes);
   P.gpart_end = P.gpart + static_cast<size_t>(ngroups) * split * 2 * (PART_BYTES / 4);
-  if (counter_bytes + static_cast<size_t>(ngroups) * split * 2 * PART_BYTES > a.scratch_bytes)
+  if (counter_bytes + sytag_bytes + static_cast<size_t>(ngroups) * split * 2 * PART_BYTES > a.scratch_bytes)
     return cudaErrorInvalidValue;
   P.N = static_cast<int>(a.N);
   P.tt = tt;
@@ -1387,7 +1420,7 @@ cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   P.neg_zero = -0.0f;
   P.flags = a.flags;
 
-  e = cudaMemsetAsync(P.counters, 0, static_cast<size_t>(ngroups) * 32, stream);
+  e = cudaMemsetAsync(P.counters, 0, counter_bytes + sytag_bytes, stream);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ngroups * split, 1, 1);

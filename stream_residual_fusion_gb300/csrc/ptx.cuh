@@ -322,6 +322,21 @@ __device__ __forceinline__ unsigned gload_acquire(const unsigned* ctr) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
   return v;
 }
+// Tagged words: a float and a 32-bit tag in one aligned 64-bit word, written with one relaxed
+// gpu-scope store. An aligned 8-byte access is single-copy atomic, so a reader that sees the tag
+// it waits for also sees the value stored with it, without any fence on either side.
+__device__ __forceinline__ void tagged_store(unsigned long long* p, float v, uint32_t tag) {
+  const uint64_t w = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t tagged_load(const unsigned long long* p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ uint32_t word_tag(uint64_t w) { return static_cast<uint32_t>(w >> 32); }
+__device__ __forceinline__ float word_value(uint64_t w) { return __uint_as_float(static_cast<uint32_t>(w)); }
+
 // Prefetch the line holding p into L1.
 __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.L1 [%0];" ::"l"(p));
