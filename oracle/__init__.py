@@ -12,7 +12,9 @@ Pages followed (cited by title and section throughout):
     (the [[3,1],[1,1]] hand check and the 1e-6 float64 criterion).
 
 mx.py holds the MXFP8 encoding of y (a format the pages leave open; the reading taken is stated
-there).
+there). backward.py holds the gradients of the step (the pages define no backward pass; the
+reading taken -- reverse-mode differentiation of the forward code with the bf16 casts passed
+straight through -- is stated there).
 
 Every function is pinned by tests under tests/ (tests/test_oracle_*.py); nothing here is
 "parity unpinned".
