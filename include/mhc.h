@@ -157,6 +157,46 @@ int mhc_fused_step_mxfp8(const void* X, const void* F, const float* pre_prev,
                          int sinkhorn_iters, float hc_eps, float norm_eps, unsigned flags,
                          void* scratch, size_t scratch_bytes, void* stream);
 
+/* ---- gradients of the step (training) -------------------------------------------------------
+ * The pages define the forward step only; no page describes a backward pass. The gradients
+ * computed are those of reverse-mode differentiation of the pages' forward code (Stream weights
+ * for the feed-forward, Code: hc_post, hc_mixes, hc_pre, hc_split_sinkhorn; MoE RMSNorm, Code:
+ * RMSNorm, Block.forward) with its casts to bf16 passed straight through, every derivative taken
+ * at the values the forward computed. Per token, with x = flat(X'), K = 4d,
+ * r = (|x|^2/K + norm_eps)^(-1/2), r_y = (|y_hat|^2/d + norm_eps)^(-1/2), T = sum gain gy y_hat:
+ *   g_m (24) from (gpre, gpost, gcomb) through the split and every Sinkhorn round;
+ *   g_y_hat = r_y gain gy - (r_y^3 T / d) y_hat;
+ *   g_X'_k = gXp_k + p_k g_y_hat + (W^T (r g_m))_k - (r^2/K)(g_m . m) X'_k;
+ *   gX_j = sum_k C_jk g_X'_k; gF = sum_k u_k g_X'_k; gpost_prev_k = g_X'_k . F;
+ *   gcomb_prev_jk = g_X'_k . X_j; gpre_prev_j = g_y_hat . X'_j;
+ *   gW = sum over tokens of (r g_m) x^T; ggain = sum of r_y gy y_hat; gbase, gscale from the split.
+ * (MHC_COMB_ROW_DEST: the other comb reading, as in the forward.)
+ * Inputs (device, layouts as for mhc_fused_step):
+ *   X, F, pre_prev, post_prev, comb_prev, W_mix [24, 4d] fp32, scale, base, gain   the forward's inputs
+ *   Xp    bf16 [N, 4, d]   the forward's X' output (saved activation)
+ *   mixes fp32 [N, 24]     the forward's mixes output m (saved activation)
+ *   gXp bf16 [N, 4, d], gy bf16 [N, d], gpre, gpost fp32 [N, 4], gcomb fp32 [N, 4, 4]
+ *                          gradients of the forward's outputs X', y, p, u, C
+ * Outputs (device): gX bf16 [N, 4, d], gF bf16 [N, d], gpre_prev, gpost_prev fp32 [N, 4],
+ *   gcomb_prev fp32 [N, 4, 4]; gW fp32 [24, 4d], gbase fp32 [24], gscale fp32 [3],
+ *   ggain fp32 [d] (sums over the N tokens; written, not accumulated; zero when N = 0).
+ * workspace: >= mhc_backward_workspace_bytes(N, n, d) device bytes, 16-byte aligned.
+ * Shapes: n = 4, d a multiple of 64, sinkhorn_iters >= 1 (MHC_ERR_SHAPE); flags other than
+ * MHC_COMB_ROW_DEST are MHC_ERR_SHAPE. No output may overlap an input or another output.
+ * Five kernels run in order on `stream`.                                                      */
+int mhc_fused_step_backward(const void* X, const void* F, const void* Xp, const float* mixes,
+                            const float* pre_prev, const float* post_prev, const float* comb_prev,
+                            const float* W_mix, const float* scale, const float* base,
+                            const float* gain, const void* gXp, const void* gy, const float* gpre,
+                            const float* gpost, const float* gcomb, void* gX, void* gF,
+                            float* gpre_prev, float* gpost_prev, float* gcomb_prev, float* gW,
+                            float* gbase, float* gscale, float* ggain, int64_t N, int n, int d,
+                            int sinkhorn_iters, float hc_eps, float norm_eps, unsigned flags,
+                            void* workspace, size_t workspace_bytes, void* stream);
+/* Workspace bytes of mhc_fused_step_backward on the current device (0 if the shape is
+ * unsupported).                                                                               */
+size_t mhc_backward_workspace_bytes(int64_t N, int n, int d);
+
 /* ---- the fused step without any allocation --------------------------------------------------
  * No counterpart in the paper: an addition for callers that cannot allocate device memory when
  * they run the step -- a serving loop that runs under a fixed device-memory budget, or whose

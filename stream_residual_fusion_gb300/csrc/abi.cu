@@ -438,6 +438,101 @@ int mhc_fused_step_noalloc(const void* X, const void* F, const float* pre_prev,
                       stream);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Gradients of the step.
+
+size_t mhc_backward_workspace_bytes(int64_t N, int n, int d) {
+  if (n != 4 || N < 0 || N > kMaxTokens || d <= 0 || d % 64 != 0) return 0;
+  return bwd_layout(N, d).bytes;
+}
+
+int mhc_fused_step_backward(const void* X, const void* F, const void* Xp, const float* mixes,
+                            const float* pre_prev, const float* post_prev, const float* comb_prev,
+                            const float* W_mix, const float* scale, const float* base,
+                            const float* gain, const void* gXp, const void* gy, const float* gpre,
+                            const float* gpost, const float* gcomb, void* gX, void* gF,
+                            float* gpre_prev, float* gpost_prev, float* gcomb_prev, float* gW,
+                            float* gbase, float* gscale, float* ggain, int64_t N, int n, int d,
+                            int sinkhorn_iters, float hc_eps, float norm_eps, unsigned flags,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (n != 4 || N < 0 || N > kMaxTokens || d <= 0 || d % 64 != 0 || sinkhorn_iters < 1)
+    return MHC_ERR_SHAPE;
+  if ((flags & ~MHC_COMB_ROW_DEST) != 0) return MHC_ERR_SHAPE;
+  if (!W_mix || !scale || !base || !gain || !gW || !gbase || !gscale || !ggain) return MHC_ERR_NULL;
+  const void* params[] = {W_mix, scale, base, gain, gW, gbase, gscale, ggain};
+  for (const void* p : params)
+    if (!aligned16(p)) return MHC_ERR_ALIGN;
+  const uint64_t nt = static_cast<uint64_t>(N), K = 4ull * d;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {   // sums over no tokens
+    const Span pin[] = {span(W_mix, 96 * K), span(scale, 12), span(base, 96), span(gain, 4ull * d)};
+    const Span pout[] = {span(gW, 96 * K), span(gbase, 96), span(gscale, 12), span(ggain, 4ull * d)};
+    if (!aliasing_ok(pout, pin)) return MHC_ERR_ALIAS;
+    cudaError_t e = cudaMemsetAsync(gW, 0, 96 * K, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(gbase, 0, 96, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(gscale, 0, 12, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ggain, 0, 4ull * d, s);
+    return cuda_code(e);
+  }
+  const void* ptrs[] = {X, F, Xp, mixes, pre_prev, post_prev, comb_prev, gXp, gy, gpre, gpost,
+                        gcomb, gX, gF, gpre_prev, gpost_prev, gcomb_prev};
+  for (const void* p : ptrs)
+    if (!p) return MHC_ERR_NULL;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MHC_ERR_ALIGN;
+  if (!workspace) return MHC_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MHC_ERR_ALIGN;
+  const size_t need = bwd_layout(N, d).bytes;
+  if (need == 0) return MHC_ERR_CUDA;
+  if (workspace_bytes < need) return MHC_ERR_WORKSPACE;
+  const Span ins[] = {span(X, nt * K * 2),      span(F, nt * d * 2),       span(Xp, nt * K * 2),
+                      span(mixes, nt * 96),     span(pre_prev, nt * 16),   span(post_prev, nt * 16),
+                      span(comb_prev, nt * 64), span(W_mix, 96 * K),       span(scale, 12),
+                      span(base, 96),           span(gain, 4ull * d),      span(gXp, nt * K * 2),
+                      span(gy, nt * d * 2),     span(gpre, nt * 16),       span(gpost, nt * 16),
+                      span(gcomb, nt * 64)};
+  const Span outs[] = {span(gX, nt * K * 2),      span(gF, nt * d * 2),     span(gpre_prev, nt * 16),
+                       span(gpost_prev, nt * 16), span(gcomb_prev, nt * 64), span(gW, 96 * K),
+                       span(gbase, 96),           span(gscale, 12),         span(ggain, 4ull * d),
+                       span(workspace, workspace_bytes)};
+  if (!aliasing_ok(outs, ins)) return MHC_ERR_ALIAS;
+  BwdArgs a{};
+  a.X = X;
+  a.F = F;
+  a.Xp = Xp;
+  a.mixes = mixes;
+  a.pre_prev = pre_prev;
+  a.post_prev = post_prev;
+  a.comb_prev = comb_prev;
+  a.W = W_mix;
+  a.scale = scale;
+  a.base = base;
+  a.gain = gain;
+  a.gXp = gXp;
+  a.gy = gy;
+  a.gpre = gpre;
+  a.gpost = gpost;
+  a.gcomb = gcomb;
+  a.gX = gX;
+  a.gF = gF;
+  a.gpre_prev = gpre_prev;
+  a.gpost_prev = gpost_prev;
+  a.gcomb_prev = gcomb_prev;
+  a.gW = gW;
+  a.gbase = gbase;
+  a.gscale = gscale;
+  a.ggain = ggain;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.N = N;
+  a.d = d;
+  a.iters = sinkhorn_iters;
+  a.hc_eps = hc_eps;
+  a.norm_eps = norm_eps;
+  a.flags = flags;
+  return cuda_code(launch_backward(a, s));
+}
+
 int mhc_set_trace(void* buffer, int64_t bytes) {
   if (buffer != nullptr && (!aligned16(buffer) || bytes < 64)) return MHC_ERR_ALIGN;
   g_trace = static_cast<unsigned long long*>(buffer);

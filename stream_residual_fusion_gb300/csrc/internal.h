@@ -100,6 +100,52 @@ cudaError_t launch_hc_post(const void* X, const void* F, const float* post, cons
 cudaError_t launch_hc_pre(const void* Xp, const float* pre, void* y_hat, int64_t N, int d,
                           cudaStream_t stream);
 
+// Gradients of the step (backward.cu).
+struct BwdArgs {
+  const void* X;          // bf16 [N, 4, d]
+  const void* F;          // bf16 [N, d]
+  const void* Xp;         // bf16 [N, 4, d], the forward's X'
+  const float* mixes;     // [N, 24], the forward's m
+  const float* pre_prev;
+  const float* post_prev;
+  const float* comb_prev;
+  const float* W;         // fp32 [24, 4d]
+  const float* scale;
+  const float* base;
+  const float* gain;
+  const void* gXp;        // bf16 [N, 4, d]
+  const void* gy;         // bf16 [N, d]
+  const float* gpre;
+  const float* gpost;
+  const float* gcomb;
+  void* gX;               // bf16 [N, 4, d]
+  void* gF;               // bf16 [N, d]
+  float* gpre_prev;
+  float* gpost_prev;
+  float* gcomb_prev;
+  float* gW;              // [24, 4d]
+  float* gbase;           // [24]
+  float* gscale;          // [3]
+  float* ggain;           // [d]
+  void* workspace;
+  size_t workspace_bytes;
+  int64_t N;
+  int d;
+  int iters;
+  float hc_eps;
+  float norm_eps;
+  unsigned flags;
+};
+// Workspace of the backward on the current device: byte offsets of its parts and the total.
+struct BwdLayout {
+  size_t off_wt, off_gm, off_rec, off_gsf, off_gpl, off_part0, off_partW, off_partG, bytes;
+  int ranges;    // token ranges of the weight-gradient partial sums
+  int blocks0;   // blocks of the mix-gradient kernel (its partial sums)
+};
+// bytes == 0 if d is not a multiple of 64 or the device cannot be queried.
+BwdLayout bwd_layout(int64_t N, int d);
+cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream);
+
 // Address ranges of the tensors of a call, for the overlap checks of the entry points.
 struct Span {
   uintptr_t lo, hi;

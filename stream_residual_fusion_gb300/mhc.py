@@ -62,6 +62,8 @@ SIGNATURES = {
     "mhc_fused_step_packed": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_fused_step_mxfp8": (_I, [_P] * 16 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
     "mhc_step_scratch_bytes": (_SZ, [_I, _I]),
+    "mhc_fused_step_backward": (_I, [_P] * 25 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _P]),
+    "mhc_backward_workspace_bytes": (_SZ, [_I64, _I, _I]),
     "mhc_fused_step_noalloc": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P]),
     "mhc_noalloc_scratch_bytes": (_SZ, []),
     "mhc_fused_step_host": (_I, [_P] * 15 + [_I64, _I, _I, _I, _F, _F, _U, _P, _SZ, _I64, _P]),
@@ -250,6 +252,52 @@ def fused_step_mxfp8(X, F, pre_prev, post_prev, comb_prev, W_packed, scale, base
         _ptr(o["pre"]), _ptr(o["post"]), _ptr(o["comb"]), _ptr(o.get("mixes")), N, n, d, iters,
         hc_eps, norm_eps, flags, _ptr(scratch), scratch.numel(), _stream(stream))
     _check(rc, "mhc_fused_step_mxfp8")
+    return o
+
+
+def backward_workspace_bytes(N: int, d: int, n: int = N_STREAMS) -> int:
+    return int(lib.mhc_backward_workspace_bytes(N, n, d))
+
+
+def fused_step_backward(X, F, Xp, mixes, pre_prev, post_prev, comb_prev, W, scale, base, gain,
+                        gXp, gy, gpre, gpost, gcomb, *, iters=20, hc_eps=1e-6, norm_eps=1e-6,
+                        flags=0, out=None, workspace=None, stream=None):
+    """mhc_fused_step_backward: gradients of the fused step. Xp and mixes are the forward's X'
+    and m outputs; gXp, gy, gpre, gpost, gcomb the gradients of its outputs. Returns dict with
+    gX, gF (bf16), gpre_prev, gpost_prev, gcomb_prev, gW, gbase, gscale, ggain (fp32)."""
+    for t, nm in ((X, "X"), (F, "F"), (Xp, "Xp"), (gXp, "gXp"), (gy, "gy")):
+        _need(t, torch.bfloat16, nm)
+    for t, nm in ((mixes, "mixes"), (pre_prev, "pre_prev"), (post_prev, "post_prev"),
+                  (comb_prev, "comb_prev"), (W, "W"), (scale, "scale"), (base, "base"),
+                  (gain, "gain"), (gpre, "gpre"), (gpost, "gpost"), (gcomb, "gcomb")):
+        _need(t, torch.float32, nm)
+    N, n, d = X.shape
+    dev = X.device
+    o = dict(out or {})
+
+    def need(key, shape, dtype):
+        if key not in o:
+            o[key] = torch.empty(shape, dtype=dtype, device=dev)
+    need("gX", (N, n, d), torch.bfloat16)
+    need("gF", (N, d), torch.bfloat16)
+    need("gpre_prev", (N, n), torch.float32)
+    need("gpost_prev", (N, n), torch.float32)
+    need("gcomb_prev", (N, n, n), torch.float32)
+    need("gW", tuple(W.shape), torch.float32)
+    need("gbase", tuple(base.shape), torch.float32)
+    need("gscale", (3,), torch.float32)
+    need("ggain", (d,), torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(1, backward_workspace_bytes(N, d, n)), dtype=torch.uint8,
+                                device=dev)
+    rc = lib.mhc_fused_step_backward(
+        _ptr(X), _ptr(F), _ptr(Xp), _ptr(mixes), _ptr(pre_prev), _ptr(post_prev), _ptr(comb_prev),
+        _ptr(W), _ptr(scale), _ptr(base), _ptr(gain), _ptr(gXp), _ptr(gy), _ptr(gpre),
+        _ptr(gpost), _ptr(gcomb), _ptr(o["gX"]), _ptr(o["gF"]), _ptr(o["gpre_prev"]),
+        _ptr(o["gpost_prev"]), _ptr(o["gcomb_prev"]), _ptr(o["gW"]), _ptr(o["gbase"]),
+        _ptr(o["gscale"]), _ptr(o["ggain"]), N, n, d, iters, hc_eps, norm_eps, flags,
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mhc_fused_step_backward")
     return o
 
 

@@ -128,3 +128,21 @@ def subset(inputs: dict, tokens) -> dict:
     unchanged. Used to hand a sample of a large batch to the oracle."""
     per_token = ("X", "F", "pre", "post", "comb")
     return {k: (v[tokens] if k in per_token else v) for k, v in inputs.items() if k != "outliers"}
+
+
+def make_upstream(N: int, n: int = N_STREAMS, d: int = WIDTH, *, seed: int, device="cpu",
+                  std: float = 1.0) -> dict:
+    """Seeded gradients of the step's outputs for the backward: gXp (of X', bf16 [N,n,d]), gy
+    (of y, bf16 [N,d]), gpre, gpost (fp32 [N,n]) and gcomb (fp32 [N,n,n]), all N(0, std^2)."""
+    dev = torch.device(device)
+
+    def g(i):
+        return _gen(dev, seed * 100 + 50 + i)
+    return {
+        "gXp": (torch.randn(N, n, d, generator=g(0), device=dev) * std).to(torch.bfloat16),
+        "gy": (torch.randn(N, d, generator=g(1), device=dev) * std).to(torch.bfloat16),
+        "gpre": torch.randn(N, n, generator=g(2), device=dev) * std,
+        "gpost": torch.randn(N, n, generator=g(3), device=dev) * std,
+        "gcomb": torch.randn(N, n, n, generator=g(4), device=dev) * std,
+    }
+
