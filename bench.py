@@ -729,6 +729,87 @@ def run_mxfp8(args):
     return 0
 
 
+# bytes per token of the backward (d = 5120, n = 4). Algorithmic, the least a single pass must
+# move: read X, F, gXp, gy and the small per-token inputs (p, u, C of the previous step, m, and
+# the gradients of p, u, C); write gX, gF and the gradients of the previous p, u, C.
+BACKWARD_BYTES_PER_TOKEN = (4 + 1 + 4 + 1) * 5120 * 2 + (4 + 1) * 5120 * 2 + 96 + 96 + 96 + 96
+# What the five kernels move: the token pass and the weight pass each read X' and gy again.
+BACKWARD_DESIGN_BYTES_PER_TOKEN = BACKWARD_BYTES_PER_TOKEN + 2 * (4 * 5120 * 2 + 5120 * 2)
+
+
+def run_backward(args):
+    """mhc_fused_step_backward on the workload (default B=4, T=8192): the gradients of every
+    input and parameter of the step from seeded gradients of its outputs, timed with CUDA events
+    per call (inputs larger than L2), against the backward's algorithmic bytes."""
+    import torch
+    from stream_residual_fusion_gb300 import mhc, synth
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    N, d = w.N, w.d
+    inp = synth.make_workload(w, seed=3000, device=dev)
+    inp.pop("outliers", None)
+    up = synth.make_upstream(N, 4, d, seed=3001, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fw = mhc.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], inp["W"],
+                        inp["scale"], inp["base"], inp["gain"], with_mixes=True, stream=stream)
+    ws = torch.empty(mhc.backward_workspace_bytes(N, d), dtype=torch.uint8, device=dev)
+    out = {}
+
+    def step():
+        return mhc.fused_step_backward(inp["X"], inp["F"], fw["Xp"], fw["mixes"], inp["pre"],
+                                       inp["post"], inp["comb"], inp["W"], inp["scale"],
+                                       inp["base"], inp["gain"], up["gXp"], up["gy"], up["gpre"],
+                                       up["gpost"], up["gcomb"], out=out or None, workspace=ws,
+                                       stream=stream)
+    out.update(step())
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    T = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(T(), T()) for _ in range(K)]
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    clk = ClockSampler(visible[dev.index].strip() if dev.index < len(visible) else dev.index)
+    clk.start()
+    time.sleep(0.3)
+    clk.mark_on()
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk.mark_off()
+    clk.stop()
+    if mhc.get_status() != mhc.MHC_OK:
+        raise RuntimeError("device-side wait gave up")
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    p50 = percentile(ms, 50)
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    alg = N * BACKWARD_BYTES_PER_TOKEN + 2 * (24 * 4 * d * 4) + 2 * d * 4
+    design = N * BACKWARD_DESIGN_BYTES_PER_TOKEN + 2 * (24 * 4 * d * 4) + 2 * d * 4
+    line = {
+        "metric": "backward of the fused mHC step tokens/s at n=4,d=5120; % of HBM roofline",
+        "form": "backward", "value": N / (p50 / 1e3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": K, "warmup": args.warmup, "ms_per_step": p50, "higher_is_better": True,
+        "dtype": "bf16 streams, fp32 parameters and gradients of parameters", "data": "synthetic",
+        "config": {"workload": f"{w.name} (N={N}), n=4, d={d}", "sinkhorn_iters": 20,
+                   "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": alg / (p50 / 1e3) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": alg / (p50 / 1e3) / 1e9 / peak, "traffic": None,
+                     "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": alg,
+                     "what": "the whole call (six launches) against the single-pass bytes"},
+        "design_bytes_per_launch": design,
+        "design_frac": design / (p50 / 1e3) / 1e9 / peak,
+        "ms_p50": p50, "ms_p95": percentile(ms, 95), "ms_p99": percentile(ms, 99),
+        "clocks": clk.summary(), "gpu_launches": K * 6,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -749,9 +830,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of the step (no host submission cost; for small workloads)")
-    ap.add_argument("--form", choices=("fused", "unfused", "mxfp8"), default="fused",
+    ap.add_argument("--form", choices=("fused", "unfused", "mxfp8", "backward"), default="fused",
                     help="unfused: time the four-kernel form beside the fused step; mxfp8: the "
-                         "step with MXFP8 y beside the bf16-y step (one GPU each)")
+                         "step with MXFP8 y beside the bf16-y step; backward: the gradients of "
+                         "the step (one GPU each)")
     ap.add_argument("--prepacked", action="store_true",
                     help="pack the weights once before timing (as a decode loop does); the step is "
                          "then the fused launch alone")
@@ -771,6 +853,8 @@ def main():
         return run_unfused(args)
     if args.form == "mxfp8":
         return run_mxfp8(args)
+    if args.form == "backward":
+        return run_backward(args)
     return run_ours(args)
 
 

@@ -26,7 +26,8 @@
 //                      accumulate); 8 consumer warps recompute X' and y_hat exactly as the forward
 //                      does, form g_X', write gX and gF in place of X and F, and accumulate gu and
 //                      gC; one warp stores gX and gF with TMA.
-//   bwd_weight_kernel  per (64-column block, token range): gW and ggain partial sums.
+//   bwd_weight_kernel  per (64-column block, token range): gW partial sums on the tensor cores
+//                      (X'^T against the planes of r g_m, both token-major), ggain beside them.
 //   bwd_reduce_kernel  sums the partials into gW, ggain, g_base, g_scale (fixed order).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -741,117 +742,244 @@ __global__ void pack_wt_kernel(const float* __restrict__ W, uint8_t* __restrict_
 }
 
 // ---------------------------------------------------------------------------------------------
-// bwd_weight_kernel: per work item (64-column block cb, token range tr), partial sums over the
-// range's tokens of gW[o][k d + c] = sum_t (r g_m)_t,o X'_t,k,c and ggain[c] = sum_t r_y gy y_hat.
+// bwd_weight_kernel: per work item (64-column block cb of all four streams, token range tr), the
+// partial sums over the range's tokens of gW[o][k d + c] = sum_t (r g_m)_t,o X'_t,k,c on the
+// tensor cores, and of ggain[c] = sum_t r_y gy_t,c y_hat_t,c on the consumer warps.
+//
+// The contraction runs over tokens, so both operands are read token-major as TMA lays them
+// down: A = X'^T (M = 128 of the block's 256 (stream, column) values, MN-major, 128-byte
+// swizzle: 64 columns of one stream per 128-byte row, two streams LBO apart, 8-token groups
+// 1 KB apart) and B = the bf16 planes of r g_m (N = 32 mix rows of which 24 are used, MN-major,
+// 64-byte swizzle). hi and lo planes accumulate into the same fp32 accumulator (X' is exact in
+// bf16). Two accumulators of [128 x 32] (streams 0-1 and 2-3) stay in TMEM for the whole range.
 
-constexpr int WT_THREADS = 256;
-constexpr int WT_TB = 32;        // tokens staged per batch
-constexpr int WT_COLS = 64;
+constexpr int WT_COLS = 64;                  // columns per work item (of each stream)
+constexpr int WT_TB = 64;                    // tokens per stage (four MMA K-steps)
+constexpr int WT_NST = 4;                    // stages
+constexpr int WT_XB = WT_TB * 128;           // one X'_k box: [64 tokens x 64 columns] bf16
+constexpr int WT_OFF_GY = 4 * WT_XB;
+constexpr int WT_OFF_GH = WT_OFF_GY + WT_XB;         // [64 tokens x 32] bf16, 64-byte rows
+constexpr int WT_OFF_GL = WT_OFF_GH + WT_TB * 64;
+constexpr int WT_OFF_P = WT_OFF_GL + WT_TB * 64;     // p_prev [64][4] fp32
+constexpr int WT_OFF_R = WT_OFF_P + WT_TB * 16;      // {r, r_y, tau, c1} [64][4] fp32
+constexpr int WT_STAGE = WT_OFF_R + WT_TB * 16;
+constexpr int WT_OFF_RED = WT_NST * WT_STAGE;        // ggain partials [4 phases][64 columns]
+constexpr int WT_OFF_BARS = WT_OFF_RED + 4 * WT_COLS * 4;
+// full, empty per stage; dfull, dfree
+constexpr int WT_NBARS = 2 * WT_NST + 2;
+constexpr int WT_OFF_TMEM = WT_OFF_BARS + WT_NBARS * 8;
+constexpr int WT_SMEM = WT_OFF_TMEM + 16 + 1024;
+static_assert(WT_STAGE % 1024 == 0, "stage alignment (128-byte swizzle)");
+static_assert(WT_SMEM <= 232448, "shared memory budget");
+constexpr int WT_CONS = 4;                   // consumer / epilogue warps (2..5)
+constexpr int WT_THREADS = (2 + WT_CONS) * 32;
+constexpr uint32_t WT_TMEM_COLS = 64;
 
-__global__ void __launch_bounds__(WT_THREADS, 2) bwd_weight_kernel(
-    const __nv_bfloat16* __restrict__ Xp, const __nv_bfloat16* __restrict__ gy,
-    const float* __restrict__ pre_prev, const float* __restrict__ rec, const float* __restrict__ gsf,
-    float* __restrict__ partW, float* __restrict__ partG, int64_t N, int d, int ranges,
-    float neg_zero) {
-  __shared__ __align__(16) uint32_t sx[WT_TB][4][WT_COLS / 2];   // X' as bf16 pairs
-  __shared__ __align__(16) uint32_t sgy[WT_TB][WT_COLS / 2];
-  __shared__ __align__(16) float sg[WT_TB][MIXN];
-  __shared__ __align__(16) float sp[WT_TB][4];
-  __shared__ float sry[WT_TB];
-  __shared__ float gred[WT_THREADS];
-  const int tid = threadIdx.x;
-  const int k = tid >> 6, cpair = (tid & 63) >> 1, oh = tid & 1;   // gW role
-  const int gcol = tid & 63, gq = tid >> 6;                         // ggain role
-  const int nblocks = d / WT_COLS;
-  const int64_t items = static_cast<int64_t>(nblocks) * ranges;
-  const int64_t per = (N + ranges - 1) / ranges;
-  const f2 nz{neg_zero, neg_zero};
-  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
-    __syncthreads();   // the previous item's reads of gred are done
-    const int cb = static_cast<int>(item % nblocks);
+// Shared-memory descriptor of an MN-major operand: `row_bytes` (64 or 128) of the MN dimension
+// per row with the swizzle of that width, consecutive K rows row_bytes apart, 8-row K groups
+// `sbo` bytes apart, the next MN atom `lbo` bytes on.
+__device__ __forceinline__ uint64_t sdesc_mnmajor(uint32_t saddr, int row_bytes, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(row_bytes == 128 ? 2 : 4) << 61);
+}
+
+struct WtParams {
+  float* partW;
+  float* partG;
+  const float* pre_prev;
+  const float* rec;
+  unsigned* status;
+  int64_t N;
+  int d;
+  int ranges;
+  int64_t per;          // tokens per range (a multiple of WT_TB)
+  float neg_zero;
+};
+
+__global__ void __launch_bounds__(WT_THREADS, 1)
+    bwd_weight_kernel(const __grid_constant__ CUtensorMap tm_xp, const __grid_constant__ CUtensorMap tm_gy,
+                      const __grid_constant__ CUtensorMap tm_gp, const WtParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + WT_OFF_BARS);
+  uint64_t* empty = full + WT_NST;
+  uint64_t* dfull = empty + WT_NST;
+  uint64_t* dfree = dfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + WT_OFF_TMEM);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblocks = P.d / WT_COLS;
+  const int64_t items = static_cast<int64_t>(nblocks) * P.ranges;
+  bool timed_out = false;
+  auto limit = [&]() { return timed_out ? 0ull : BWD_WAIT_NS; };
+  // batches of an item: its token range cut into stages of WT_TB tokens
+  auto range_of = [&](int64_t item, int64_t& t0, int64_t& t1) {
     const int tr = static_cast<int>(item / nblocks);
-    const int64_t tb0 = tr * per, tb1 = std::min<int64_t>(N, tb0 + per);
-    float acc[2][12];
+    t0 = tr * P.per;
+    t1 = std::min<int64_t>(P.N, t0 + P.per);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < WT_NST; ++b) {
+      mbar_init(&full[b], 1);
+      mbar_init(&empty[b], 1 + WT_CONS);
+    }
+    mbar_init(dfull, 1);
+    mbar_init(dfree, WT_CONS);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, WT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_xp);
+      tma_prefetch_desc(&tm_gy);
+      tma_prefetch_desc(&tm_gp);
+      const uint64_t pol = policy_evict_first();
+      int g = 0;
+      for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+        const int cb = static_cast<int>(item % nblocks);
+        int64_t t0, t1;
+        range_of(item, t0, t1);
+        for (int64_t tb = t0; tb < t1; tb += WT_TB, ++g) {
+          const int b = g % WT_NST;
+          if (g >= WT_NST && !mbar_wait(&empty[b], ((g / WT_NST) - 1) & 1, limit())) timed_out = true;
+          const uint32_t nt = static_cast<uint32_t>(std::min<int64_t>(WT_TB, P.N - tb));
+          uint8_t* st = sm + b * WT_STAGE;
+          // the boxes always move WT_TB rows (rows past N read as zero); p and rec move nt rows
+          mbar_arrive_expect_tx(&full[b], 5u * WT_XB + 2u * WT_TB * 64 + 2u * nt * 16);
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int o = 0; o < 12; ++o) acc[a][o] = 0.f;
-    float gacc = 0.f;
-    for (int64_t t0 = tb0; t0 < tb1; t0 += WT_TB) {
-      const int nt = static_cast<int>(std::min<int64_t>(WT_TB, tb1 - t0));
-      __syncthreads();
-      // stage: X' (4 streams x 64 columns = 4 x 8 uint4 per token), gy (8 uint4), r g_m (6
-      // float4), p (1 float4), r_y
-      for (int i = tid; i < WT_TB * 32; i += WT_THREADS) {
-        const int tk = i >> 5, kk = (i >> 3) & 3, ch = i & 7;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tk < nt)
-          v = __ldg(reinterpret_cast<const uint4*>(Xp + ((t0 + tk) * 4 + kk) * static_cast<int64_t>(d) + cb * WT_COLS) + ch);
-        reinterpret_cast<uint4*>(&sx[tk][kk][0])[ch] = v;
-      }
-      for (int i = tid; i < WT_TB * 8; i += WT_THREADS) {
-        const int tk = i >> 3, ch = i & 7;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tk < nt) v = __ldg(reinterpret_cast<const uint4*>(gy + (t0 + tk) * static_cast<int64_t>(d) + cb * WT_COLS) + ch);
-        reinterpret_cast<uint4*>(&sgy[tk][0])[ch] = v;
-      }
-      for (int i = tid; i < WT_TB * 6; i += WT_THREADS) {
-        const int tk = i / 6, ch = i % 6;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (tk < nt) v = __ldg(reinterpret_cast<const float4*>(gsf + (t0 + tk) * MIXN) + ch);
-        reinterpret_cast<float4*>(&sg[tk][0])[ch] = v;
-      }
-      if (tid < WT_TB) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        float ry = 0.f;
-        if (tid < nt) {
-          v = __ldg(reinterpret_cast<const float4*>(pre_prev) + t0 + tid);
-          ry = __ldg(rec + (t0 + tid) * 4 + 1);
+          for (int k = 0; k < 4; ++k)
+            tma_load_3d_hint(st + k * WT_XB, &tm_xp, &full[b], cb * WT_COLS, k, static_cast<int>(tb), pol);
+          tma_load_2d_hint(st + WT_OFF_GY, &tm_gy, &full[b], cb * WT_COLS, static_cast<int>(tb), pol);
+          tma_load_2d(st + WT_OFF_GH, &tm_gp, &full[b], 0, static_cast<int>(tb));
+          tma_load_2d(st + WT_OFF_GL, &tm_gp, &full[b], 32, static_cast<int>(tb));
+          bulk_load_hint(st + WT_OFF_P, P.pre_prev + tb * 4, nt * 16, &full[b], pol);
+          bulk_load_hint(st + WT_OFF_R, P.rec + tb * 4, nt * 16, &full[b], pol);
         }
-        *reinterpret_cast<float4*>(&sp[tid][0]) = v;
-        sry[tid] = ry;
-      }
-      __syncthreads();
-      for (int tk = 0; tk < nt; ++tk) {
-        const f2 x = bf2_to_f2(sx[tk][k][cpair]);
-        const float4* gp = reinterpret_cast<const float4*>(&sg[tk][12 * oh]);
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const float4 g = gp[q];
-          const float gv[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc[0][4 * q + e] = fmaf(gv[e], x.x, acc[0][4 * q + e]);
-            acc[1][4 * q + e] = fmaf(gv[e], x.y, acc[1][4 * q + e]);
-          }
-        }
-      }
-      // ggain of column gcol over tokens gq, gq + 4, ...: y_hat recomputed as the forward does
-      for (int tk = gq; tk < nt; tk += 4) {
-        const float4 p = *reinterpret_cast<const float4*>(&sp[tk][0]);
-        const f2 cpv[4] = {f2{p.x, p.x}, f2{p.y, p.y}, f2{p.z, p.z}, f2{p.w, p.w}};
-        f2 xp[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) xp[kk] = bf2_to_f2(sx[tk][kk][gcol >> 1]);
-        const f2 yh = bf2_to_f2(f2_to_bf2(hc_pre_pair(cpv, xp, nz)));
-        const f2 g = bf2_to_f2(sgy[tk][gcol >> 1]);
-        const float yv = (gcol & 1) ? yh.y : yh.x;
-        const float gv = (gcol & 1) ? g.y : g.x;
-        gacc = fmaf(gv * sry[tk], yv, gacc);
       }
     }
-    // partials: gW block of range tr, [o][4d] row-major
-    float* pw = partW + static_cast<int64_t>(tr) * MIXN * 4 * d;
-    const int64_t c0 = static_cast<int64_t>(k) * d + cb * WT_COLS + 2 * cpair;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // bf16 A and B, fp32 D, M = 128, N = 32, both operands MN-major
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 32) | (1u << 15) | (1u << 16);
+      int g = 0, it = 0;
+      for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+        int64_t t0, t1;
+        range_of(item, t0, t1);
+        // the epilogue has read the previous item's accumulators
+        if (it > 0 && !mbar_wait(dfree, (it - 1) & 1, limit())) timed_out = true;
+        tc_fence_after();
+        bool first = true;
+        for (int64_t tb = t0; tb < t1; tb += WT_TB, ++g) {
+          const int b = g % WT_NST;
+          if (!mbar_wait(&full[b], (g / WT_NST) & 1, limit())) timed_out = true;
+          tc_fence_after();
+          const uint32_t st = smem_u32(sm + b * WT_STAGE);
 #pragma unroll
-    for (int o = 0; o < 12; ++o)
-      *reinterpret_cast<float2*>(pw + static_cast<int64_t>(12 * oh + o) * 4 * d + c0) = make_float2(acc[0][o], acc[1][o]);
-    gred[tid] = gacc;
-    __syncthreads();
-    if (tid < WT_COLS)
-      partG[static_cast<int64_t>(tr) * d + cb * WT_COLS + tid] =
-          (gred[tid] + gred[tid + 64]) + (gred[tid + 128] + gred[tid + 192]);
+          for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int pl = 0; pl < 2; ++pl) {
+#pragma unroll
+              for (int ks = 0; ks < WT_TB / 16; ++ks) {
+                const uint64_t a = sdesc_mnmajor(st + 2 * mt * WT_XB + ks * 2048, 128, WT_XB, 1024);
+                const uint64_t bd = sdesc_mnmajor(st + (pl ? WT_OFF_GL : WT_OFF_GH) + ks * 1024, 64, 0, 512);
+                umma_bf16(tmem + static_cast<uint32_t>(mt * 32), a, bd, idesc,
+                          (first && pl == 0 && ks == 0) ? 0u : 1u);
+              }
+            }
+          }
+          first = false;
+          umma_commit(&empty[b]);
+        }
+        umma_commit(dfull);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ ggain and epilogue
+    const int ct = threadIdx.x - 64;            // 0..127
+    const int cp = ct & 31;                     // column pair: columns 2cp, 2cp+1 of the block
+    const int ph = ct >> 5;                     // tokens ph, ph + 4, ...
+    const int q = warp & 3;                     // TMEM lane quarter
+    const f2 nz{P.neg_zero, P.neg_zero};
+    float* red = reinterpret_cast<float*>(sm + WT_OFF_RED);
+    int g = 0, it = 0;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
+      const int cb = static_cast<int>(item % nblocks);
+      const int tr = static_cast<int>(item / nblocks);
+      int64_t t0, t1;
+      range_of(item, t0, t1);
+      f2 gacc{0.f, 0.f};
+      for (int64_t tb = t0; tb < t1; tb += WT_TB, ++g) {
+        const int b = g % WT_NST;
+        if (!mbar_wait(&full[b], (g / WT_NST) & 1, limit())) timed_out = true;
+        const int nt = static_cast<int>(std::min<int64_t>(WT_TB, t1 - tb));
+        const uint8_t* st = sm + b * WT_STAGE;
+        const float* sp = reinterpret_cast<const float*>(st + WT_OFF_P);
+        const float* sr = reinterpret_cast<const float*>(st + WT_OFF_R);
+        for (int t = ph; t < nt; t += 4) {
+          // column pair cp of token row t in a 128-byte-swizzled box
+          const uint32_t off = static_cast<uint32_t>(t * 128) +
+                               ((static_cast<uint32_t>((cp >> 2) ^ (t & 7))) << 4) + (cp & 3) * 4;
+          f2 xp[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) xp[k] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(st + k * WT_XB + off));
+          const float4 p = *reinterpret_cast<const float4*>(sp + 4 * t);
+          const f2 cpv[4] = {f2{p.x, p.x}, f2{p.y, p.y}, f2{p.z, p.z}, f2{p.w, p.w}};
+          const f2 yh = bf2_to_f2(f2_to_bf2(hc_pre_pair(cpv, xp, nz)));
+          const f2 gyv = bf2_to_f2(*reinterpret_cast<const uint32_t*>(st + WT_OFF_GY + off));
+          const float ry = sr[4 * t + 1];
+          gacc = fma2(mul2(gyv, f2{ry, ry}), yh, gacc);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[b]);
+      }
+      // gW partials of the range: accumulator mt holds (stream 2mt + m / 64, column m % 64) in
+      // TMEM lane m, mix row o in column 32 mt + o
+      if (!mbar_wait(dfull, it & 1, limit())) timed_out = true;
+      tc_fence_after();
+      float* pw = P.partW + static_cast<int64_t>(tr) * MIXN * 4 * P.d;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 32), v);
+        if (t1 <= t0) {   // a range past the last token: no MMA ran, its sums are zero
+#pragma unroll
+          for (int o = 0; o < 32; ++o) v[o] = 0u;
+        }
+        const int m = q * 32 + lane;
+        const int64_t col = static_cast<int64_t>(2 * mt + (m >> 6)) * P.d + cb * WT_COLS + (m & 63);
+#pragma unroll
+        for (int o = 0; o < MIXN; ++o) pw[static_cast<int64_t>(o) * 4 * P.d + col] = __uint_as_float(v[o]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dfree);
+      // ggain partials of the range: the four token phases of each column added in order
+      red[ph * WT_COLS + 2 * cp] = gacc.x;
+      red[ph * WT_COLS + 2 * cp + 1] = gacc.y;
+      named_bar_sync(1, WT_CONS * 32);
+      if (ct < WT_COLS)
+        P.partG[static_cast<int64_t>(tr) * P.d + cb * WT_COLS + ct] =
+            (red[ct] + red[WT_COLS + ct]) + (red[2 * WT_COLS + ct] + red[3 * WT_COLS + ct]);
+      named_bar_sync(1, WT_CONS * 32);
+    }
   }
+
+  if (timed_out) atomicOr(P.status, STATUS_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, WT_TMEM_COLS);
 }
 
 // Sums of the partials: gW [24][4d], ggain [d] over `ranges`, g_base [24] and g_scale [3] over
@@ -913,6 +1041,13 @@ bool bmap_streams(CUtensorMap* m, const void* p, int64_t N, int d, uint32_t rows
   const cuuint32_t box[3] = {BDC, 1, rows};
   return bmap(m, p, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
+bool bmap_streams_box(CUtensorMap* m, const void* p, int64_t N, int d, uint32_t cols, uint32_t rows,
+                      CUtensorMapSwizzle swz) {   // [N, 4, d], boxes of [rows x cols] of one stream
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), 4, static_cast<cuuint64_t>(N)};
+  const cuuint64_t str[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 8};
+  const cuuint32_t box[3] = {cols, 1, rows};
+  return bmap(m, p, 3, dims, str, box, swz);
+}
 bool bmap_rows(CUtensorMap* m, const void* p, int64_t N, int cols, uint32_t box_cols, uint32_t rows,
                CUtensorMapSwizzle swz) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(N)};
@@ -938,11 +1073,14 @@ BwdLayout bwd_layout(int64_t N, int d) {
   BwdLayout L{};
   const int sms = sm_count();
   if (sms <= 0 || d <= 0 || d % WT_COLS != 0) return L;
-  const int grid = 2 * sms;
+  const int grid = sms;
   const int nblocks = d / WT_COLS;
   int ranges = grid / gcd_i(grid, nblocks);
   ranges = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({static_cast<int64_t>(ranges), 64,
                                                                      (N + WT_TB - 1) / WT_TB})));
+  // tokens per range: a multiple of the stage height, so only the last range ends in a partial
+  // stage (whose rows past N read as zero)
+  L.per = std::max<int64_t>(WT_TB, ((N + ranges - 1) / ranges + WT_TB - 1) / WT_TB * WT_TB);
   L.ranges = ranges;
   L.blocks0 = static_cast<int>(std::max<int64_t>(1, (N + MIX_THREADS - 1) / MIX_THREADS));
   size_t off = 0;
@@ -1035,11 +1173,28 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   {
+    CUtensorMap txp, tgy, tgp;
+    if (!bmap_streams_box(&txp, a.Xp, N, d, WT_COLS, WT_TB, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !bmap_rows(&tgy, a.gy, N, d, WT_COLS, WT_TB, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !bmap_rows(&tgp, ws + L.off_gpl, N, 64, 32, WT_TB, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+    WtParams W{};
+    W.partW = wsf(L.off_partW);
+    W.partG = wsf(L.off_partG);
+    W.pre_prev = a.pre_prev;
+    W.rec = wsf(L.off_rec);
+    W.status = status;
+    W.N = N;
+    W.d = d;
+    W.ranges = L.ranges;
+    W.per = L.per;
+    W.neg_zero = -0.0f;
     const int64_t items = static_cast<int64_t>(d / WT_COLS) * L.ranges;
-    const int blocks = static_cast<int>(std::min<int64_t>(items, 2 * sms));
-    bwd_weight_kernel<<<blocks, WT_THREADS, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.Xp), static_cast<const __nv_bfloat16*>(a.gy), a.pre_prev,
-        wsf(L.off_rec), wsf(L.off_gsf), wsf(L.off_partW), wsf(L.off_partG), N, d, L.ranges, -0.0f);
+    e = cudaFuncSetAttribute(bwd_weight_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, WT_SMEM);
+    if (e != cudaSuccess) return e;
+    bwd_weight_kernel<<<static_cast<int>(std::min<int64_t>(items, sms)), WT_THREADS, WT_SMEM, stream>>>(txp, tgy, tgp, W);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
   {
     const int64_t total = static_cast<int64_t>(MIXN) * 4 * d + d + MIXN + 3;

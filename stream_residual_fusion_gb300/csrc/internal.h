@@ -140,6 +140,7 @@ struct BwdArgs {
 struct BwdLayout {
   size_t off_wt, off_gm, off_rec, off_gsf, off_gpl, off_part0, off_partW, off_partG, bytes;
   int ranges;    // token ranges of the weight-gradient partial sums
+  int64_t per;   // tokens per range
   int blocks0;   // blocks of the mix-gradient kernel (its partial sums)
 };
 // bytes == 0 if d is not a multiple of 64 or the device cannot be queried.
