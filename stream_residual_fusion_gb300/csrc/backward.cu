@@ -55,19 +55,26 @@ constexpr int MIX_THREADS = 64;
 constexpr int CK_EVERY = 8;         // least Sinkhorn checkpoint spacing (steps)
 constexpr int CK_MAX = 6;           // checkpoints held per token (shared memory)
 
+// Reciprocal of a positive normal float within 1 ulp (the hardware approximation).
+__device__ __forceinline__ float rcp_fast(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // One Sinkhorn normalisation of c in place: step i even divides columns, odd divides rows.
 __device__ __forceinline__ void sk_step(float (&c)[16], int i, float eps) {
   if ((i & 1) == 0) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float r = 1.0f / (((c[k] + c[4 + k]) + (c[8 + k] + c[12 + k])) + eps);
+      const float r = rcp_fast(((c[k] + c[4 + k]) + (c[8 + k] + c[12 + k])) + eps);
 #pragma unroll
       for (int j = 0; j < 4; ++j) c[4 * j + k] *= r;
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float r = 1.0f / (((c[4 * j] + c[4 * j + 1]) + (c[4 * j + 2] + c[4 * j + 3])) + eps);
+      const float r = rcp_fast(((c[4 * j] + c[4 * j + 1]) + (c[4 * j + 2] + c[4 * j + 3])) + eps);
 #pragma unroll
       for (int k = 0; k < 4; ++k) c[4 * j + k] *= r;
     }
@@ -81,7 +88,7 @@ __device__ __forceinline__ void sk_step_back(float (&g)[16], const float (&c)[16
     for (int k = 0; k < 4; ++k) {
       const float s = ((c[k] + c[4 + k]) + (c[8 + k] + c[12 + k])) + eps;
       const float gc = (g[k] * c[k] + g[4 + k] * c[4 + k]) + (g[8 + k] * c[8 + k] + g[12 + k] * c[12 + k]);
-      const float inv = 1.0f / s;
+      const float inv = rcp_fast(s);
       const float t = gc * inv * inv;
 #pragma unroll
       for (int j = 0; j < 4; ++j) g[4 * j + k] = g[4 * j + k] * inv - t;
@@ -93,7 +100,7 @@ __device__ __forceinline__ void sk_step_back(float (&g)[16], const float (&c)[16
       float* gr = g + 4 * j;
       const float s = ((cr[0] + cr[1]) + (cr[2] + cr[3])) + eps;
       const float gc = (gr[0] * cr[0] + gr[1] * cr[1]) + (gr[2] * cr[2] + gr[3] * cr[3]);
-      const float inv = 1.0f / s;
+      const float inv = rcp_fast(s);
       const float t = gc * inv * inv;
 #pragma unroll
       for (int k = 0; k < 4; ++k) gr[k] = gr[k] * inv - t;
@@ -432,7 +439,9 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       tma_prefetch_desc(&tm_f);
       tma_prefetch_desc(&tm_gxp);
       tma_prefetch_desc(&tm_gy);
-      const uint64_t pol = policy_evict_first();
+      // normal eviction priority: each CTA reads its slots one after another, so a tile's rows
+      // stay in L2 between the slots that read them (measured 9% faster than evict-first)
+      const uint64_t pol = policy_evict_normal();
       const uint32_t bytes = 10u * static_cast<uint32_t>(tt * BROWB);
       int gs = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -994,6 +1003,7 @@ __global__ void bwd_reduce_kernel(const float* __restrict__ partW, const float* 
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float v = 0.f;
     if (i < nW) {
+#pragma unroll 8
       for (int r = 0; r < ranges; ++r) v += partW[r * nW + i];
       gW[i] = v;
     } else if (i < nW + d) {
@@ -1026,13 +1036,15 @@ PFN_cuTensorMapEncodeTiled_v12000 bwd_encode_fn() {
   return fn;
 }
 
+// No L2 promotion: a CTA of these kernels reads the neighbouring columns of a row only slots
+// later, so fetching them early only adds traffic.
 bool bmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
           const cuuint32_t* box, CUtensorMapSwizzle swz) {
   auto fn = bwd_encode_fn();
   if (fn == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 bool bmap_streams(CUtensorMap* m, const void* p, int64_t N, int d, uint32_t rows) {   // [N, 4, d]
