@@ -294,6 +294,16 @@ def run_table(args):
     return 0
 
 
+def workload_config(w, n_total: int, n_rank: int) -> dict:
+    """The workload both arms report (the reference arm's oracle runs a bounded sample of it,
+    described in its cpu_baseline.sample)."""
+    return {"workload": f"{w.name} (N={n_total}), n=4, d={w.d}", "B": w.B, "T": w.T, "n": 4,
+            "d": w.d, "tokens_per_rank": n_rank, "sinkhorn_iters": 20,
+            "comb_reading": "code: X'_k = u_k F + sum_j C_jk X_j",
+            "l2": (f"inputs larger than L2 ({n_rank * 51200 / 1e9:.2f} GB of streams read per step)"
+                   if n_rank * 51200 > 129e6 else "inputs smaller than L2 (not flushed)")}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -316,8 +326,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * wall / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name + " (N=32768), n=4, d=5120", "B": w.B, "T": w.T, "n": 4,
-                   "d": w.d, "sample": "bounded per step: see cpu_baseline.sample"},
+        "config": workload_config(w, w.N, w.N),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -510,12 +519,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": args.scaling, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name} (N={N_total}), n=4, d={d}", "B": w.B, "T": w.T, "n": 4, "d": d,
-                   "tokens_per_rank": N,
-                   "sinkhorn_iters": 20, "comb_reading": "code: X'_k = u_k F + sum_j C_jk X_j",
-                   "l2": (f"inputs larger than L2 ({N * 51200 / 1e9:.2f} GB of streams read per step)"
-                          if N * 51200 > 129e6 else "inputs smaller than L2 (not flushed)"),
-                   "step": (("CUDA-graph replay of " if args.graph else "") +
+        "config": workload_config(w, N_total, N),
+        "launch": {"step": (("CUDA-graph replay of " if args.graph else "") +
                             ("mhc_fused_step_packed (weights packed once, before timing)"
                              if args.prepacked else "mhc_pack_weights + mhc_fused_step_packed")),
                    "launch_shape": dict(zip(("split", "tile", "groups"),
