@@ -25,7 +25,7 @@
 //                      (A = the tile's planes of r g_m, B = the slot's planes of W^T, fp32
 //                      accumulate); 8 consumer warps recompute X' and y_hat exactly as the forward
 //                      does, form g_X', write gX and gF in place of X and F, and accumulate gu and
-//                      gC; one warp stores gX and gF with TMA.
+//                      gC; a second lane of the producer warp stores gX and gF with TMA.
 //   bwd_weight_kernel  per (64-column block, token range): gW partial sums on the tensor cores
 //                      (X'^T against the planes of r g_m, both token-major), ggain beside them.
 //   bwd_reduce_kernel  sums the partials into gW, ggain, g_base, g_scale (fixed order).
@@ -349,8 +349,7 @@ constexpr int BSMEM = BOFF_TMEM + 16 + 1024;
 static_assert(BSMEM <= 232448, "shared memory budget");
 static_assert(BSTAGE % 1024 == 0 && BWB % 1024 == 0 && BOFF_A % 1024 == 0, "tile alignment");
 constexpr int BNCONS = 8;
-constexpr int BSTORE = 2 + BNCONS;           // warp 10
-constexpr int BTHREADS = (BSTORE + 1) * 32;
+constexpr int BTHREADS = (2 + BNCONS) * 32;
 constexpr uint32_t BTMEM_COLS = 256;         // two [128 x 128] fp32 accumulators
 
 __host__ __device__ constexpr int bx_tile(int b, int k) { return b * BSTAGE + k * BTILE; }       // X_k
@@ -460,6 +459,27 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           tma_load_2d_hint(sm + by_tile(b), &tm_gy, &full[b], col, t0, pol);
         }
       }
+    } else if (lane == 1) {
+      // -------------------------------------------------------------- gX / gF stores
+      tma_prefetch_desc(&tm_gx);
+      tma_prefetch_desc(&tm_gf);
+      const uint64_t pol = policy_evict_first();
+      int gs = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int t0 = tile * tt;
+        for (int s = 0; s < S; ++s, ++gs) {
+          const int b = gs % BNST;
+          if (!mbar_wait(&xready[b], (gs / BNST) & 1, limit())) timed_out = true;
+          const int col = s * BDC;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tma_store_3d_hint(&tm_gx, sm + bx_tile(b, k), col, k, t0, pol);
+          tma_store_2d_hint(&tm_gf, sm + bf_tile(b), col, t0, pol);
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(&empty[b]);
+        }
+      }
+      bulk_wait<0>();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -512,29 +532,6 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           load_a(tile + gridDim.x);
         }
       }
-    }
-  } else if (warp == BSTORE) {
-    // ------------------------------------------------------------------ gX / gF stores
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_gx);
-      tma_prefetch_desc(&tm_gf);
-      const uint64_t pol = policy_evict_first();
-      int gs = 0;
-      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int t0 = tile * tt;
-        for (int s = 0; s < S; ++s, ++gs) {
-          const int b = gs % BNST;
-          if (!mbar_wait(&xready[b], (gs / BNST) & 1, limit())) timed_out = true;
-          const int col = s * BDC;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) tma_store_3d_hint(&tm_gx, sm + bx_tile(b, k), col, k, t0, pol);
-          tma_store_2d_hint(&tm_gf, sm + bf_tile(b), col, t0, pol);
-          bulk_commit();
-          bulk_wait_read<0>();
-          mbar_arrive(&empty[b]);
-        }
-      }
-      bulk_wait<0>();
     }
   } else {
     // ------------------------------------------------------------------ consumers
@@ -991,31 +988,50 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, WT_TMEM_COLS);
 }
 
-// Sums of the partials: gW [24][4d], ggain [d] over `ranges`, g_base [24] and g_scale [3] over
-// the mix kernel's blocks. One thread per output, in a fixed order.
-__global__ void bwd_reduce_kernel(const float* __restrict__ partW, const float* __restrict__ partG,
-                                  const float* __restrict__ part0, float* __restrict__ gW,
-                                  float* __restrict__ ggain, float* __restrict__ gbase,
-                                  float* __restrict__ gscale, int d, int ranges, int blocks0) {
-  const int64_t nW = static_cast<int64_t>(MIXN) * 4 * d;
-  const int64_t total = nW + d + MIXN + 3;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+// Sums of the partials in a fixed order: gW [24][4d] and ggain [d] over `ranges` (four
+// consecutive outputs per thread, one float4 load per range), and in the last block g_base [24]
+// and g_scale [3] over the mix kernel's blocks (eight strided partial sums per output, then
+// added in order).
+__global__ void __launch_bounds__(256) bwd_reduce_kernel(
+    const float* __restrict__ partW, const float* __restrict__ partG, const float* __restrict__ part0,
+    float* __restrict__ gW, float* __restrict__ ggain, float* __restrict__ gbase,
+    float* __restrict__ gscale, int d, int ranges, int blocks0) {
+  if (blockIdx.x == gridDim.x - 1) {
+    __shared__ float red[8][32];
+    const int j = threadIdx.x & 31, q = threadIdx.x >> 5;
     float v = 0.f;
-    if (i < nW) {
-#pragma unroll 8
-      for (int r = 0; r < ranges; ++r) v += partW[r * nW + i];
-      gW[i] = v;
-    } else if (i < nW + d) {
-      const int64_t c = i - nW;
-      for (int r = 0; r < ranges; ++r) v += partG[r * static_cast<int64_t>(d) + c];
-      ggain[c] = v;
-    } else {
-      const int j = static_cast<int>(i - nW - d);
-      for (int b = 0; b < blocks0; ++b) v += part0[static_cast<int64_t>(b) * 32 + j];
-      if (j < MIXN) gbase[j] = v;
-      else gscale[j - MIXN] = v;
+    if (j < MIXN + 3)
+      for (int b = q; b < blocks0; b += 8) v += part0[static_cast<int64_t>(b) * 32 + j];
+    red[q][j] = v;
+    __syncthreads();
+    if (threadIdx.x < MIXN + 3) {
+      float t = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t += red[k][threadIdx.x];
+      if (threadIdx.x < MIXN) gbase[threadIdx.x] = t;
+      else gscale[threadIdx.x - MIXN] = t;
     }
+    return;
+  }
+  const int64_t nW4 = static_cast<int64_t>(MIXN) * d;     // float4s of gW (24 x 4d floats)
+  const int64_t nG4 = d / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nW4 + nG4;
+       i += static_cast<int64_t>(gridDim.x - 1) * blockDim.x) {
+    const bool w = i < nW4;
+    const float4* src = w ? reinterpret_cast<const float4*>(partW) + i
+                          : reinterpret_cast<const float4*>(partG) + (i - nW4);
+    const int64_t stride = w ? nW4 : nG4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int r = 0; r < ranges; ++r) {
+      const float4 p = __ldg(src + r * stride);
+      v.x += p.x;
+      v.y += p.y;
+      v.z += p.z;
+      v.w += p.w;
+    }
+    if (w) reinterpret_cast<float4*>(gW)[i] = v;
+    else reinterpret_cast<float4*>(ggain)[i - nW4] = v;
   }
 }
 
@@ -1209,8 +1225,8 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   {
-    const int64_t total = static_cast<int64_t>(MIXN) * 4 * d + d + MIXN + 3;
-    const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 8 * sms));
+    const int64_t total4 = static_cast<int64_t>(MIXN) * d + d / 4;
+    const int blocks = static_cast<int>(std::min<int64_t>((total4 + 255) / 256, 4 * sms)) + 1;
     bwd_reduce_kernel<<<blocks, 256, 0, stream>>>(wsf(L.off_partW), wsf(L.off_partG), wsf(L.off_part0), a.gW,
                                                   a.ggain, a.gbase, a.gscale, d, L.ranges, L.blocks0);
   }
