@@ -20,8 +20,9 @@
 //   bwd_token_kernel   one warp per token: the token reductions over X' and gy (|x|^2, |y_hat|^2,
 //                      T, and gain gy . X'_j, y_hat . X'_j for gp), the per-token scalars and the
 //                      two bf16 planes of r g_m that the stream kernel's tensor cores read.
-//   bwd_stream_kernel  one CTA per 128-token tile, all columns, in slots of 32: a TMA ring brings
-//                      X, F, gXp and gy; one thread issues tcgen05.mma for W^T (r g_m) into TMEM
+//   bwd_stream_kernel  one CTA per token tile (up to 112 tokens), all columns, in slots of 32: two
+//                      TMA rings bring X, F (freed once gX, gF written over them are stored) and
+//                      gXp, gy (freed once read); one thread issues tcgen05.mma for W^T (r g_m) into TMEM
 //                      (A = the tile's planes of r g_m, B = the slot's planes of W^T, fp32
 //                      accumulate); 8 consumer warps recompute X' and y_hat exactly as the forward
 //                      does, form g_X', write gX and gF in place of X and F, and accumulate gu and
@@ -328,34 +329,40 @@ __global__ void __launch_bounds__(TOK_THREADS) bwd_token_kernel(
 // ---------------------------------------------------------------------------------------------
 // bwd_stream_kernel
 
-constexpr int BT = 128;                      // token rows of a tile (the MMA's M)
+constexpr int BT = 128;                      // the MMA's M: rows of its A operand and of D
+constexpr int BTR = 112;                     // token rows of a tile (at most): the ring tiles' height
 constexpr int BDC = 32;                      // columns per slot
 constexpr int BROWB = BDC * 2;               // 64-byte tile rows (64-byte swizzle)
-constexpr int BTILE = BT * BROWB;            // one [128 x 32] bf16 tile
-constexpr int BSTAGE = 10 * BTILE;           // X_0..3, F, gXp_0..3, gy
-constexpr int BNST = 2;
+constexpr int BTILE = BTR * BROWB;           // one [112 x 32] bf16 tile
+constexpr int BSETB = 5 * BTILE;             // five tiles: X_0..3 and F, or gXp_0..3 and gy
+// Two rings, by how long a slot's tiles are held: X and F are written over by gX and gF and freed
+// once the stores have read them; gXp and gy are freed as soon as the consumers have read them.
+constexpr int BNA = 3;                       // X/F entries
+constexpr int BNB = 2;                       // gXp/gy entries
 constexpr int BWB = 128 * 128;               // W^T planes of a slot: 128 rows (stream, column) x 128 B
-constexpr int BNW = 2;
+constexpr int BNW = 1;                       // weight entries (refilled once a slot's MMAs are done)
 constexpr int BAB = BT * 128;                // the tile's planes of r g_m: 128 rows x 128 B
-constexpr int BOFF_W = BNST * BSTAGE;
+constexpr int BOFF_B = BNA * BSETB;
+constexpr int BOFF_W = BOFF_B + BNB * BSETB;
 constexpr int BOFF_A = BOFF_W + BNW * BWB;
 constexpr int BOFF_RED = BOFF_A + BAB;       // [BT][20] partial sums of the tile's second threads
 constexpr int BOFF_BARS = BOFF_RED + BT * 20 * 4;
-// full, empty, xready per stage; wfull, wempty per weight entry; dready, dfree per TMEM buffer;
-// afull, aempty
-constexpr int BNBARS = 3 * BNST + 2 * BNW + 4 + 2;
+// fullA, emptyA, xready per X/F entry; fullB, emptyB per gXp/gy entry; wfull, wempty per weight
+// entry; dready, dfree per TMEM buffer; afull, aempty
+constexpr int BNBARS = 3 * BNA + 2 * BNB + 2 * BNW + 4 + 2;
 constexpr int BOFF_TMEM = BOFF_BARS + BNBARS * 8;
 constexpr int BSMEM = BOFF_TMEM + 16 + 1024;
 static_assert(BSMEM <= 232448, "shared memory budget");
-static_assert(BSTAGE % 1024 == 0 && BWB % 1024 == 0 && BOFF_A % 1024 == 0, "tile alignment");
+static_assert(BTILE % 512 == 0 && BSETB % 1024 == 0 && BWB % 1024 == 0 && BOFF_A % 1024 == 0,
+              "tile alignment");
 constexpr int BNCONS = 8;
 constexpr int BTHREADS = (2 + BNCONS) * 32;
 constexpr uint32_t BTMEM_COLS = 256;         // two [128 x 128] fp32 accumulators
 
-__host__ __device__ constexpr int bx_tile(int b, int k) { return b * BSTAGE + k * BTILE; }       // X_k
-__host__ __device__ constexpr int bf_tile(int b) { return b * BSTAGE + 4 * BTILE; }              // F
-__host__ __device__ constexpr int bg_tile(int b, int k) { return b * BSTAGE + (5 + k) * BTILE; } // gXp_k
-__host__ __device__ constexpr int by_tile(int b) { return b * BSTAGE + 9 * BTILE; }              // gy
+__host__ __device__ constexpr int bx_tile(int a, int k) { return a * BSETB + k * BTILE; }            // X_k
+__host__ __device__ constexpr int bf_tile(int a) { return a * BSETB + 4 * BTILE; }                   // F
+__host__ __device__ constexpr int bg_tile(int b, int k) { return BOFF_B + b * BSETB + k * BTILE; }   // gXp_k
+__host__ __device__ constexpr int by_tile(int b) { return BOFF_B + b * BSETB + 4 * BTILE; }          // gy
 
 struct BwdParams {
   const float* pre_prev;
@@ -383,10 +390,12 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + BOFF_BARS);
-  uint64_t* empty = full + BNST;
-  uint64_t* xready = empty + BNST;
-  uint64_t* wfull = xready + BNST;
+  uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + BOFF_BARS);
+  uint64_t* emptyA = fullA + BNA;
+  uint64_t* xready = emptyA + BNA;
+  uint64_t* fullB = xready + BNA;
+  uint64_t* emptyB = fullB + BNB;
+  uint64_t* wfull = emptyB + BNB;
   uint64_t* wempty = wfull + BNW;
   uint64_t* dready = wempty + BNW;
   uint64_t* dfree = dready + 2;
@@ -405,10 +414,14 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   const int total = my_tiles * S;   // this CTA's slots
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < BNST; ++b) {
-      mbar_init(&full[b], 1);
-      mbar_init(&empty[b], 1);
-      mbar_init(&xready[b], BNCONS);
+    for (int a = 0; a < BNA; ++a) {
+      mbar_init(&fullA[a], 1);
+      mbar_init(&emptyA[a], 1);
+      mbar_init(&xready[a], BNCONS);
+    }
+    for (int b = 0; b < BNB; ++b) {
+      mbar_init(&fullB[b], 1);
+      mbar_init(&emptyB[b], BNCONS);
     }
     for (int e = 0; e < BNW; ++e) {
       mbar_init(&wfull[e], 1);
@@ -441,22 +454,23 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       // normal eviction priority: each CTA reads its slots one after another, so a tile's rows
       // stay in L2 between the slots that read them (measured 9% faster than evict-first)
       const uint64_t pol = policy_evict_normal();
-      const uint32_t bytes = 10u * static_cast<uint32_t>(tt * BROWB);
+      const uint32_t bytes = 5u * static_cast<uint32_t>(tt * BROWB);   // five tt-row boxes
       int gs = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int t0 = tile * tt;
         for (int s = 0; s < S; ++s, ++gs) {
-          const int b = gs % BNST;
-          if (gs >= BNST && !mbar_wait(&empty[b], ((gs / BNST) - 1) & 1, limit())) timed_out = true;
+          const int a = gs % BNA, b = gs % BNB;
           const int col = s * BDC;
-          mbar_arrive_expect_tx(&full[b], bytes);
+          if (gs >= BNA && !mbar_wait(&emptyA[a], ((gs / BNA) - 1) & 1, limit())) timed_out = true;
+          mbar_arrive_expect_tx(&fullA[a], bytes);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            tma_load_3d_hint(sm + bx_tile(b, k), &tm_x, &full[b], col, k, t0, pol);
-            tma_load_3d_hint(sm + bg_tile(b, k), &tm_gxp, &full[b], col, k, t0, pol);
-          }
-          tma_load_2d_hint(sm + bf_tile(b), &tm_f, &full[b], col, t0, pol);
-          tma_load_2d_hint(sm + by_tile(b), &tm_gy, &full[b], col, t0, pol);
+          for (int k = 0; k < 4; ++k) tma_load_3d_hint(sm + bx_tile(a, k), &tm_x, &fullA[a], col, k, t0, pol);
+          tma_load_2d_hint(sm + bf_tile(a), &tm_f, &fullA[a], col, t0, pol);
+          if (gs >= BNB && !mbar_wait(&emptyB[b], ((gs / BNB) - 1) & 1, limit())) timed_out = true;
+          mbar_arrive_expect_tx(&fullB[b], bytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tma_load_3d_hint(sm + bg_tile(b, k), &tm_gxp, &fullB[b], col, k, t0, pol);
+          tma_load_2d_hint(sm + by_tile(b), &tm_gy, &fullB[b], col, t0, pol);
         }
       }
     } else if (lane == 1) {
@@ -468,15 +482,15 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int t0 = tile * tt;
         for (int s = 0; s < S; ++s, ++gs) {
-          const int b = gs % BNST;
-          if (!mbar_wait(&xready[b], (gs / BNST) & 1, limit())) timed_out = true;
+          const int a = gs % BNA;
+          if (!mbar_wait(&xready[a], (gs / BNA) & 1, limit())) timed_out = true;
           const int col = s * BDC;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tma_store_3d_hint(&tm_gx, sm + bx_tile(b, k), col, k, t0, pol);
-          tma_store_2d_hint(&tm_gf, sm + bf_tile(b), col, t0, pol);
+          for (int k = 0; k < 4; ++k) tma_store_3d_hint(&tm_gx, sm + bx_tile(a, k), col, k, t0, pol);
+          tma_store_2d_hint(&tm_gf, sm + bf_tile(a), col, t0, pol);
           bulk_commit();
           bulk_wait_read<0>();
-          mbar_arrive(&empty[b]);
+          mbar_arrive(&emptyA[a]);
         }
       }
       bulk_wait<0>();
@@ -540,9 +554,13 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     const int h = c >> 2;                // which 16 columns of the slot
     const int tl = sub * 32 + lane;      // token row of the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    // Threads whose row is past the tiles' height (tl >= 112) read the first rows of the next
+    // buffer in shared memory (no token of theirs is ever stored) and write nothing.
+    const bool inrows = tl < BTR;
     uint32_t row_off[2];
 #pragma unroll
     for (int q = 0; q < 2; ++q) row_off[q] = tile_chunk_offset(tl, 2 * h + q);
+    auto at = [&](int tile_off, int q) { return sm + tile_off + row_off[q]; };
     const f2 nz{P.neg_zero, P.neg_zero};
     const bool row_dest = (P.flags & 1u) != 0;
     float* red = reinterpret_cast<float*>(sm + BOFF_RED) + tl * 20;
@@ -592,8 +610,9 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         for (int j = 0; j < 4; ++j) acc_c[j][k] = 0.f;
       }
       for (int s = 0; s < S; ++s, ++gs) {
-        const int b = gs % BNST, db = gs & 1;
-        if (!mbar_wait(&full[b], (gs / BNST) & 1, limit())) timed_out = true;
+        const int a = gs % BNA, b = gs % BNB, db = gs & 1;
+        if (!mbar_wait(&fullA[a], (gs / BNA) & 1, limit())) timed_out = true;
+        if (!mbar_wait(&fullB[b], (gs / BNB) & 1, limit())) timed_out = true;
         if (!mbar_wait(&dready[db], (gs >> 1) & 1, limit())) timed_out = true;
         tc_fence_after();
 #pragma unroll
@@ -606,15 +625,15 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           uint32_t xa[4][4], fa[4], ga[4][4], ya[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint4 v = *reinterpret_cast<const uint4*>(sm + bx_tile(b, k) + row_off[q]);
+            const uint4 v = *reinterpret_cast<const uint4*>(at(bx_tile(a, k), q));
             xa[k][0] = v.x; xa[k][1] = v.y; xa[k][2] = v.z; xa[k][3] = v.w;
-            const uint4 g = *reinterpret_cast<const uint4*>(sm + bg_tile(b, k) + row_off[q]);
+            const uint4 g = *reinterpret_cast<const uint4*>(at(bg_tile(b, k), q));
             ga[k][0] = g.x; ga[k][1] = g.y; ga[k][2] = g.z; ga[k][3] = g.w;
           }
           {
-            const uint4 v = *reinterpret_cast<const uint4*>(sm + bf_tile(b) + row_off[q]);
+            const uint4 v = *reinterpret_cast<const uint4*>(at(bf_tile(a), q));
             fa[0] = v.x; fa[1] = v.y; fa[2] = v.z; fa[3] = v.w;
-            const uint4 y = *reinterpret_cast<const uint4*>(sm + by_tile(b) + row_off[q]);
+            const uint4 y = *reinterpret_cast<const uint4*>(at(by_tile(b), q));
             ya[0] = y.x; ya[1] = y.y; ya[2] = y.z; ya[3] = y.w;
           }
           const int col = s * BDC + 16 * h + 8 * q;
@@ -665,15 +684,18 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(sm + bx_tile(b, k) + row_off[q]) = make_uint4(ox[k][0], ox[k][1], ox[k][2], ox[k][3]);
-          *reinterpret_cast<uint4*>(sm + bf_tile(b) + row_off[q]) = make_uint4(of[0], of[1], of[2], of[3]);
+            if (inrows) *reinterpret_cast<uint4*>(at(bx_tile(a, k), q)) = make_uint4(ox[k][0], ox[k][1], ox[k][2], ox[k][3]);
+          if (inrows) *reinterpret_cast<uint4*>(at(bf_tile(a), q)) = make_uint4(of[0], of[1], of[2], of[3]);
         }
         tc_fence_before();   // the TMEM loads above, before the MMA that reuses the buffer
         __syncwarp();
-        if (lane == 0) mbar_arrive(&dfree[db]);
+        if (lane == 0) {
+          mbar_arrive(&dfree[db]);
+          mbar_arrive(&emptyB[b]);   // this warp has read the slot's gXp and gy
+        }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xready[b]);
+        if (lane == 0) mbar_arrive(&xready[a]);
       }
       // the token's gu and gC: the second thread's partial sums through shared memory
       if (h == 1) {
@@ -1159,9 +1181,9 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream) {
 
   // stream kernel: tile height that balances the tiles over the SMs
   {
-    int best_tt = BT;
+    int best_tt = BTR;
     int64_t best = INT64_MAX;
-    for (int tt = BT; tt >= 8; tt -= 8) {
+    for (int tt = BTR; tt >= 8; tt -= 8) {
       const int64_t tiles = (N + tt - 1) / tt;
       const int64_t rounds = (tiles + sms - 1) / sms;
       const int64_t cost = rounds * (tt + 32);
