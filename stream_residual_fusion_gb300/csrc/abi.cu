@@ -482,9 +482,6 @@ int mhc_fused_step_backward(const void* X, const void* F, const void* Xp, const 
     if (!aligned16(p)) return MHC_ERR_ALIGN;
   if (!workspace) return MHC_ERR_WORKSPACE;
   if (!aligned16(workspace)) return MHC_ERR_ALIGN;
-  const size_t need = bwd_layout(N, d).bytes;
-  if (need == 0) return MHC_ERR_CUDA;
-  if (workspace_bytes < need) return MHC_ERR_WORKSPACE;
   const Span ins[] = {span(X, nt * K * 2),      span(F, nt * d * 2),       span(Xp, nt * K * 2),
                       span(mixes, nt * 96),     span(pre_prev, nt * 16),   span(post_prev, nt * 16),
                       span(comb_prev, nt * 64), span(W_mix, 96 * K),       span(scale, 12),
@@ -496,6 +493,9 @@ int mhc_fused_step_backward(const void* X, const void* F, const void* Xp, const 
                        span(gbase, 96),           span(gscale, 12),         span(ggain, 4ull * d),
                        span(workspace, workspace_bytes)};
   if (!aliasing_ok(outs, ins)) return MHC_ERR_ALIAS;
+  const size_t need = bwd_layout(N, d).bytes;
+  if (need == 0) return MHC_ERR_CUDA;
+  if (workspace_bytes < need) return MHC_ERR_WORKSPACE;
   BwdArgs a{};
   a.X = X;
   a.F = F;

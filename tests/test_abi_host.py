@@ -230,3 +230,38 @@ def test_host_chunk_plan(M):
             assert sum(got) == N and all(1 <= x <= c for x in got)
     buf = (ctypes.c_int64 * 2)()
     assert M.lib.mhc_host_chunks(1500, 256, buf, 2) == 11 and list(buf) == [32, 64]
+
+
+def _bwd(M, N=256, n=4, d=5120, iters=20, flags=0, ptrs=None, ws=None, ws_bytes=1 << 40):
+    p = [_addr(i) for i in range(25)] if ptrs is None else ptrs
+    ws = _addr(30) if ws is None else ws
+    return M.lib.mhc_fused_step_backward(*p, N, n, d, iters, 1e-6, 1e-6, flags, ws, ws_bytes,
+                                         None)
+
+
+def test_backward_validation(M):
+    """mhc_fused_step_backward checks its arguments on the host before anything runs: shapes
+    (n = 4, d a multiple of 64, N >= 0, iters >= 1), flags, NULL and unaligned pointers, the
+    workspace, and overlap of any output with an input or another output."""
+    assert _bwd(M, n=3) == M.MHC_ERR_SHAPE
+    assert _bwd(M, N=-1) == M.MHC_ERR_SHAPE
+    assert _bwd(M, iters=0) == M.MHC_ERR_SHAPE
+    assert _bwd(M, d=5120 + 32) == M.MHC_ERR_SHAPE
+    assert _bwd(M, flags=0x2) == M.MHC_ERR_SHAPE
+    for i in (0, 3, 7, 11, 16, 21, 24):       # X, mixes, W_mix, gXp, gX, gW, ggain
+        p = [_addr(k) for k in range(25)]
+        p[i] = None
+        assert _bwd(M, ptrs=p) == M.MHC_ERR_NULL, i
+    p = [_addr(k) for k in range(25)]
+    p[2] = ctypes.c_void_p(p[2].value + 4)     # X' not 16-byte aligned
+    assert _bwd(M, ptrs=p) == M.MHC_ERR_ALIGN
+    assert _bwd(M, ws=ctypes.c_void_p(0)) == M.MHC_ERR_WORKSPACE
+    p = [_addr(k) for k in range(25)]
+    p[16] = p[0]                                # gX written over X
+    assert _bwd(M, ptrs=p) == M.MHC_ERR_ALIAS
+    p = [_addr(k) for k in range(25)]
+    p[17] = ctypes.c_void_p(p[16].value + 64)   # gF inside gX
+    assert _bwd(M, ptrs=p) == M.MHC_ERR_ALIAS
+    assert M.lib.mhc_backward_workspace_bytes(256, 4, 5120 + 32) == 0
+    assert M.lib.mhc_backward_workspace_bytes(256, 3, 5120) == 0
+

@@ -156,3 +156,41 @@ def test_backward_bench_workload_sampled(M, synth):
         g = to64(got[k])
         worst = float(np.abs(g - r).max() / (np.abs(r).max() + 1e-30))
         assert worst <= 2e-4, (k, worst)
+
+
+@pytest.mark.parametrize("N,d", [(1, 256), (129, 512), (300, 5120)])
+def test_backward_outputs_stay_in_bounds(M, synth, N, d):
+    """Every output of the backward sits at the start of a larger buffer filled with a sentinel:
+    after the call nothing past the output's end has changed, ragged token counts included, and
+    the inputs are unchanged."""
+    inp = synth.make_inputs(N, 4, d, seed=7400 + N, device=DEV, scale_uniform=True)
+    up = synth.make_upstream(N, 4, d, seed=7401 + N, device=DEV)
+    fw = M.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], inp["W"],
+                      inp["scale"], inp["base"], inp["gain"], with_mixes=True)
+    pad = 4096
+    shapes = {"gX": ((N, 4, d), torch.bfloat16), "gF": ((N, d), torch.bfloat16),
+              "gpre_prev": ((N, 4), torch.float32), "gpost_prev": ((N, 4), torch.float32),
+              "gcomb_prev": ((N, 4, 4), torch.float32), "gW": (tuple(inp["W"].shape), torch.float32),
+              "gbase": ((24,), torch.float32), "gscale": ((3,), torch.float32),
+              "ggain": ((d,), torch.float32)}
+    big, out = {}, {}
+    for k, (shape, dt) in shapes.items():
+        n = 1
+        for v in shape:
+            n *= v
+        big[k] = torch.full((n + pad,), -7.0, dtype=dt, device=DEV)
+        out[k] = big[k][:n].view(shape)
+    before = {k: v.clone() for k, v in list(inp.items()) + list(up.items()) if torch.is_tensor(v)}
+    M.fused_step_backward(inp["X"], inp["F"], fw["Xp"], fw["mixes"], inp["pre"], inp["post"],
+                          inp["comb"], inp["W"], inp["scale"], inp["base"], inp["gain"],
+                          up["gXp"], up["gy"], up["gpre"], up["gpost"], up["gcomb"], out=out)
+    torch.cuda.synchronize()
+    assert M.get_status() == M.MHC_OK
+    for k, b in big.items():
+        n = b.numel() - pad
+        assert bool((b[n:] == -7.0).all()), k
+        assert bool(torch.isfinite(b[:n].float()).all()), k
+    for k, v in before.items():
+        src = inp.get(k, up.get(k))
+        assert torch.equal(src, v), k
+    _check(out, _oracle(inp, up, 20, False))
