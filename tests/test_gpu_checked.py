@@ -3,8 +3,8 @@ access of the fused step tests its index first, skips a failing one and reports 
 
   * On valid inputs no check fires: parity with the oracle across launch shapes, ragged tails
     and both y forms, with sentinel padding around every output left untouched.
-  * With MHC_DEBUG_PLANT_OOB (accepted by this build only) one finisher row and one MXFP8 scale
-    row of the first CTA get an index N rows past the end: the checks skip those stores, the
+  * With MHC_DEBUG_PLANT_OOB (accepted by the bounds-checked library only) one finisher row and
+    one MXFP8 scale row of the first CTA get an index N rows past the end: the checks skip those stores, the
     status reports MHC_ERR_BOUNDS, the padding (larger than N rows, so even an unchecked store
     would have stayed inside this test's own buffer) is untouched, and every other output
     matches the regular build.
