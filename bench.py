@@ -380,7 +380,10 @@ def run_ours(args):
 
     # launch-shape flags (default: the library's automatic choice)
     shape_flags = ((mhc.split_flag(args.split) if args.split else 0) |
-                   (mhc.tile_flag(args.tile) if args.tile else 0))
+                   (mhc.tile_flag(args.tile) if args.tile else 0) |
+                   {"auto": 0, "persistent": mhc.PATH_PERSISTENT, "cluster": mhc.PATH_CLUSTER}[args.path])
+    path = "cluster" if mhc.step_path(N, d, shape_flags) == mhc.PATH_CLUSTER else "persistent"
+    kernel_name = "cluster_step_kernel" if path == "cluster" else "step_kernel<true>"
     if args.prepacked:
         mhc.pack_weights(inp["W"], out=Wp, stream=stream)
 
@@ -523,13 +526,14 @@ def run_ours(args):
         "launch": {"step": (("CUDA-graph replay of " if args.graph else "") +
                             ("mhc_fused_step_packed (weights packed once, before timing)"
                              if args.prepacked else "mhc_pack_weights + mhc_fused_step_packed")),
+                   "path": path,
                    "launch_shape": dict(zip(("split", "tile", "groups"),
                                             mhc.step_config(N, d, shape_flags)[:3]))},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / 8000.0,
-                     "kernel": ("step_kernel<true> (fused), timed with the packing as one graph replay"
-                                if args.graph and not args.prepacked else "step_kernel<true> (fused)"),
+                     "kernel": (f"{kernel_name} (fused), timed with the packing as one graph replay"
+                                if args.graph and not args.prepacked else f"{kernel_name} (fused)"),
                      "kernel_ms_avg": fused_avg,
                      "algorithmic_bytes_per_launch": algorithmic_bytes(N, d)},
         "kernel_percentiles": {
@@ -846,6 +850,9 @@ def main():
                     help="force the CTAs per tile (MHC_SPLIT flags); 0 = automatic")
     ap.add_argument("--tile", type=int, default=0,
                     help="force the tokens per tile (MHC_TILE flags); 0 = automatic")
+    ap.add_argument("--path", choices=("auto", "persistent", "cluster"), default="auto",
+                    help="kernel of the fused step (MHC_PATH flags): the library's choice, the "
+                         "persistent kernel, or the cluster kernel (one cluster per 40 tokens)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="synthetic workload (default: the B=4,T=8192 prefill; others are for profiling)")
     args = ap.parse_args()

@@ -65,6 +65,26 @@ extern "C" {
  * are MHC_ERR_SHAPE; the height must be a multiple of the split). 0 = automatic (above).      */
 #define MHC_TILE_SHIFT           16
 #define MHC_TILE_MASK            (0x1Fu << MHC_TILE_SHIFT)
+/* Launch path of the fused step with bf16 y (mhc_fused_step, _packed, _noalloc). Two kernels
+ * compute the same step (X' bit for bit; the other outputs within the stated tolerances, their
+ * partial sums being added in another order):
+ *   the persistent kernel: one cooperative launch, one CTA per SM; groups of `split` CTAs walk
+ *     128-token tiles and sum their partial results through the step scratch (L2);
+ *   the cluster kernel: one thread-block cluster of 16 CTAs (8 where d needs it) per tile of
+ *     40 tokens, summing through distributed shared memory; d / (32 x cluster size) <= 10
+ *     (d = 5120: 16 CTAs of 320 columns). Made for small batches (decode).
+ * Default (neither bit): the cluster kernel when d fits it and every tile's cluster runs at once
+ * on the device (up to 280 tokens at d = 5120 on a 152-SM GB300: 7 clusters of 16 CTAs), the
+ * persistent kernel otherwise, and
+ * always the persistent kernel when the split or tile bits are set.
+ * MHC_PATH_PERSISTENT: always the persistent kernel.
+ * MHC_PATH_CLUSTER: always the cluster kernel, for any N (clusters beyond what the device runs
+ *   at once wait for a free place); the split bits then choose its cluster size (0: 16 where d
+ *   fits, else 8; 4 = 8 CTAs; 5 = 16 CTAs); MHC_ERR_SHAPE with the tile bits, with
+ *   MHC_PATH_PERSISTENT, where d fits no cluster size, or in calls without bf16 y (mhc_mixes,
+ *   mhc_fused_step_mxfp8). The cluster kernel ignores the step scratch.                      */
+#define MHC_PATH_PERSISTENT      0x8u
+#define MHC_PATH_CLUSTER         0x10u
 
 /* ---- sizes ------------------------------------------------------------------------------- */
 /* Bytes of the packed projection weights (3 bf16 planes of W_mix plus padding, in the layout
@@ -137,14 +157,15 @@ int mhc_fused_step_packed(const void* X, const void* F, const float* pre_prev,
 /* ---- the fused step with y quantised for the next sublayer ----------------------------------
  * The pages name an FP4/FP8 MoE as a consumer of y ("2A · Single-Pass mHC", section 2, the flow
  * diagram) but define no quantised format; this entry writes y in the OCP Microscaling (MX) v1.0
- * format MXFP8 instead of bf16, fused into the same single pass. Everything else is as in
- * mhc_fused_step_packed (same X', p, u, C and optional mixes, bit for bit).
+ * format MXFP8 instead of bf16, fused into the same single pass. It runs the persistent kernel;
+ * everything else is as in mhc_fused_step_packed with MHC_PATH_PERSISTENT (same X', p, u, C and
+ * optional mixes, bit for bit).
  *   y_codes  uint8 [N, d]       E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
  *                                no infinities)
  *   y_scale  uint8 [N, d / 32]  E8M0 codes: block b of token t (features 32b .. 32b + 31) has
  *                                scale X = 2^(y_scale[t, b] - 127)
- * The encoded values are the bf16 y that mhc_fused_step_packed returns for the same inputs (bit
- * for bit), so the codes equal a separate MXFP8 pass over that y: X = 2^(floor(log2(amax)) - 8)
+ * The encoded values are the bf16 y that mhc_fused_step_packed returns with MHC_PATH_PERSISTENT
+ * for the same inputs (bit for bit), so the codes equal a separate MXFP8 pass over that y: X = 2^(floor(log2(amax)) - 8)
  * with amax the block's largest |y| (code clamped to >= 0; an all-zero block takes code 0); each
  * code is y / X rounded to the nearest E4M3 value, ties to even, saturating at +-448.
  * Dequantised: y ~= value(code) * X.
@@ -314,9 +335,14 @@ int mhc_get_status(void* stream);
  * exchange access of the fused step tests its index first and skips it on failure, reporting
  * MHC_ERR_BOUNDS), 0 for the regular build (the tests compiled away).                          */
 int mhc_checked_build(void);
+/* The kernel mhc_fused_step runs for N tokens of width d with `flags` on the current device:
+ * MHC_PATH_PERSISTENT or MHC_PATH_CLUSTER (see the flags above), or a negative code.          */
+int mhc_step_path(int64_t N, int n, int d, unsigned flags);
+
 /* Launch shape of the fused step (and of mhc_mixes) for N tokens of width d with `flags` on
  * the current device: CTAs that share a tile, tokens per tile, and groups launched (each group
- * is `split` CTAs, one per SM). Diagnostic; needs a GPU.                                      */
+ * is `split` CTAs, one per SM). On the cluster path (mhc_step_path): the cluster size, 40, and
+ * the number of clusters. Diagnostic; needs a GPU.                                           */
 int mhc_step_config(int64_t N, int n, int d, unsigned flags, int* split, int* tile, int* groups);
 /* Phase tracing of the fused step (off by default). With a device buffer set, every later
  * launch whose grid fits records, per CTA, 8 uint64 values from the GPU's nanosecond timer:

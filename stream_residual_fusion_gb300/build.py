@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmhc.so")
 LIB_CHECKED = os.path.join(PKG, "libmhc_checked.so")
-SOURCES = ["fused.cu", "small.cu", "abi.cu", "host_pipeline.cu", "backward.cu"]
+SOURCES = ["fused.cu", "cluster.cu", "small.cu", "abi.cu", "host_pipeline.cu", "backward.cu"]
 HEADERS = ["ptx.cuh", "mix_math.cuh", "hc_arith.cuh", "internal.h", "layout.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

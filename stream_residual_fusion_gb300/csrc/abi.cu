@@ -50,11 +50,19 @@ using namespace mhc;
 namespace {
 
 // Checks shared by the fused step and the mixes call. Returns MHC_OK and the split, or a code.
-int check_step_shape(int64_t N, int n, int d, int iters, unsigned flags, int* split) {
+// cluster_ok: the call has the cluster kernel (the fused step with bf16 y); MHC_PATH_CLUSTER is
+// MHC_ERR_SHAPE elsewhere, and where d fits no cluster size (its split bits then pick 8 or 16).
+int check_step_shape(int64_t N, int n, int d, int iters, unsigned flags, int* split,
+                     bool cluster_ok = false) {
   if (n != 4 || N < 0 || N > kMaxTokens || iters < 1 || d <= 0) return MHC_ERR_SHAPE;
   if (!MHC_CHECKED && (flags & FLAG_PLANT_OOB) != 0) return MHC_ERR_SHAPE;   // checked build only
   const int fs = split_flag_value(flags), ft = tile_flag(flags);
   if (fs < 0 || ft < 0) return MHC_ERR_SHAPE;
+  if ((flags & FLAG_PATH_CLUSTER) != 0) {
+    if (!cluster_ok || (flags & FLAG_PATH_PERSISTENT) != 0 || ft != 0) return MHC_ERR_SHAPE;
+    *split = cluster_size_for(d, fs);
+    return *split != 0 ? MHC_OK : MHC_ERR_SHAPE;
+  }
   *split = choose_split(d, fs);
   if (*split == 0) return MHC_ERR_SHAPE;
   // some split that fits d must also divide a forced tile height
@@ -76,7 +84,7 @@ int fused_common(const void* X, const void* F, const float* pre_prev, const floa
   // y_scale set: y_out receives MXFP8 E4M3 codes [N, d] (one byte each) and y_scale the E8M0
   // block scales [N, d / 32]; otherwise y_out is bf16 [N, d].
   int split = 0;
-  int rc = check_step_shape(N, n, d, iters, flags, &split);
+  int rc = check_step_shape(N, n, d, iters, flags, &split, y_scale == nullptr);
   if (rc != MHC_OK) return rc;
   if (N == 0) return MHC_OK;  // nothing to read or write (empty tensors may have no address)
   if (!X || !F || !pre_prev || !post_prev || !comb_prev || !W_packed || !scale || !base || !gain ||
@@ -184,7 +192,7 @@ int mhc_fused_step(const void* X, const void* F, const float* pre_prev, const fl
                    int64_t N, int n, int d, int sinkhorn_iters, float hc_eps, float norm_eps,
                    unsigned flags, void* workspace, size_t workspace_bytes, void* stream) {
   int split = 0;
-  const int rc = check_step_shape(N, n, d, sinkhorn_iters, flags, &split);
+  const int rc = check_step_shape(N, n, d, sinkhorn_iters, flags, &split, true);
   if (rc != MHC_OK) return rc;
   if (N == 0) return MHC_OK;
   if (!W_mix) return MHC_ERR_NULL;
@@ -359,11 +367,25 @@ const char* mhc_strerror(int code) {
   }
 }
 
+int mhc_step_path(int64_t N, int n, int d, unsigned flags) {
+  int sp = 0;
+  const int rc = check_step_shape(N, n, d, 1, flags, &sp, true);
+  if (rc != MHC_OK) return rc;
+  return cluster_path(N, d, flags, true) != 0 ? static_cast<int>(MHC_PATH_CLUSTER)
+                                              : static_cast<int>(MHC_PATH_PERSISTENT);
+}
+
 int mhc_step_config(int64_t N, int n, int d, unsigned flags, int* split, int* tile, int* groups) {
   if (!split || !tile || !groups) return MHC_ERR_NULL;
   int sp = 0, ctas = 0;
-  const int rc = check_step_shape(N, n, d, 1, flags, &sp);
+  const int rc = check_step_shape(N, n, d, 1, flags, &sp, true);
   if (rc != MHC_OK) return rc;
+  if (const int cl = cluster_path(N, d, flags, true)) {
+    *split = cl;
+    *tile = kClusterTile;
+    *groups = static_cast<int>((std::max<int64_t>(N, 1) + kClusterTile - 1) / kClusterTile);
+    return MHC_OK;
+  }
   if (step_resident_ctas(&ctas) != cudaSuccess) return MHC_ERR_CUDA;
   const StepShape sh = choose_shape(N, d, ctas, split_flag_value(flags), tile_flag(flags));
   if (sh.split == 0) return MHC_ERR_CUDA;
@@ -421,7 +443,7 @@ int mhc_fused_step_noalloc(const void* X, const void* F, const float* pre_prev,
                            float* mixes_out, int64_t N, int n, int d, int sinkhorn_iters,
                            float hc_eps, float norm_eps, unsigned flags, void* stream) {
   int split = 0;
-  int rc = check_step_shape(N, n, d, sinkhorn_iters, flags, &split);
+  int rc = check_step_shape(N, n, d, sinkhorn_iters, flags, &split, true);
   if (rc != MHC_OK) return rc;
   if (N == 0) return MHC_OK;
   if (!W_mix) return MHC_ERR_NULL;

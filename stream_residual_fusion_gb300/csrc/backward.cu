@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  block_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -729,7 +729,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
 
   if (timed_out) atomicOr(P.status, STATUS_TIMEOUT);
   tc_fence_before();
-  __syncthreads();
+  block_sync();
   if (warp == 1) tmem_dealloc(tmem, BTMEM_COLS);
 }
 
@@ -862,7 +862,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  block_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -1006,7 +1006,7 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
 
   if (timed_out) atomicOr(P.status, STATUS_TIMEOUT);
   tc_fence_before();
-  __syncthreads();
+  block_sync();
   if (warp == 1) tmem_dealloc(tmem, WT_TMEM_COLS);
 }
 
@@ -1060,25 +1060,11 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(
 // ---------------------------------------------------------------------------------------------
 // host side
 
-PFN_cuTensorMapEncodeTiled_v12000 bwd_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // No L2 promotion: a CTA of these kernels reads the neighbouring columns of a row only slots
 // later, so fetching them early only adds traffic.
 bool bmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
           const cuuint32_t* box, CUtensorMapSwizzle swz) {
-  auto fn = bwd_encode_fn();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,

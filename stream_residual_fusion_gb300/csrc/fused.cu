@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  block_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -1205,8 +1205,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (timed_out) atomicOr(P.status, STATUS_TIMEOUT);
 
   // ------------------------------------------------------------------ leave together
+  // (every warp, all its lanes included, has arrived: the TMEM is free after this)
   tc_fence_before();
-  __syncthreads();
+  block_sync();
   if (threadIdx.x == 0 && P.trace != nullptr) {
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -1224,23 +1225,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ---------------------------------------------------------------------------------------------
 // host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
               const cuuint64_t* strides, const cuuint32_t* box) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   constexpr CUtensorMapSwizzle swz = ROWB == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
@@ -1254,7 +1241,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 // MXFP8 codes of y [N, d], one byte each: boxes of DC bytes x box_rows, 32-byte swizzle.
 bool map_codes(CUtensorMap* m, const void* p, int64_t N, int d, uint32_t box_rows) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N)};
   const cuuint64_t str[1] = {static_cast<cuuint64_t>(d)};
@@ -1300,6 +1287,20 @@ cudaError_t resident_ctas(Kern kern, int* ctas) {
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
 
 bool split_ok(int d, int s) {
   // slices of whole slots, at least 128 columns (the previous tile's RMS factor
@@ -1352,6 +1353,9 @@ size_t step_scratch_bytes() {
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream) {
   const bool mx = fused && a.y_scale != nullptr;
+  // small batches: one thread-block cluster per tile (cluster.cu)
+  if (const int cl = cluster_path(a.N, a.d, a.flags, fused && !mx)) return launch_cluster_step(a, cl, stream);
+  if ((a.flags & FLAG_PATH_CLUSTER) != 0) return cudaErrorInvalidConfiguration;
   auto kern = mx ? step_kernel<true, true> : fused ? step_kernel<true> : step_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;

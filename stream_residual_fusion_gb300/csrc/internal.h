@@ -1,6 +1,8 @@
 // internal.h -- host-side declarations shared by the library's translation units.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "layout.cuh"
@@ -83,6 +85,25 @@ inline int split_flag_value(unsigned flags) {
   return v == 0 ? 0 : (v <= 6 ? 1 << (v - 1) : -1);
 }
 constexpr int kMaxTokens = 65535 * 128;
+
+// Launch-path flags (MHC_PATH_PERSISTENT, MHC_PATH_CLUSTER).
+constexpr unsigned FLAG_PATH_PERSISTENT = 0x8u;
+constexpr unsigned FLAG_PATH_CLUSTER = 0x10u;
+// The cluster kernel (cluster.cu): CTAs per cluster (16 or 8, `forced` if nonzero) whose tiles
+// fit width d, 0 if none; clusters of that size the current device runs at once (0 if it cannot
+// run one); the cluster size the step takes for (N, d, flags) (0: the persistent kernel), with
+// fused_bf16 false for the mixes-only and MXFP8 forms; and the launch.
+int cluster_size_for(int d, int forced);
+int cluster_capacity(int cl);
+int cluster_path(int64_t N, int d, unsigned flags, bool fused_bf16);
+cudaError_t launch_cluster_step(const StepArgs& a, int cl, cudaStream_t stream);
+// Automatic choice: the cluster kernel while the tiles need at most this many waves of clusters.
+constexpr int kClusterWaves = 1;
+// Tokens per tile of the cluster kernel.
+constexpr int kClusterTile = 40;
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once; nullptr if absent.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 cudaError_t launch_step(bool fused, const StepArgs& a, cudaStream_t stream);
 // CTAs of the step kernel the current device holds at once (one per SM).

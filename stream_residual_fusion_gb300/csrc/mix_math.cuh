@@ -115,22 +115,22 @@ __device__ __forceinline__ void split_sinkhorn_row(const float (&mrow)[4], float
 // The same arithmetic as split_sinkhorn_row with one lane holding the whole 4 x 4 matrix (no
 // shuffles: each column sum is ((c0 + c1) + (c2 + c3)) over the rows, the value the row
 // version's butterfly leaves in every lane), so the two give bitwise the same result. Lanes that
-// run it on the same token hold the same result. Inputs: the 24 mix numbers m. Outputs: p, u,
-// comb.
+// run it on the same token hold the same result. Inputs: the 24 mix numbers m, the split's
+// scales s0..s2 and biases b. Outputs: p, u, comb.
 __device__ __forceinline__ void split_sinkhorn_all(const float (&m)[24], float s0, float s1,
-                                                   float s2, const float* __restrict__ base,
-                                                   int iters, float eps, float (&p)[4],
-                                                   float (&u)[4], float (&c)[16]) {
+                                                   float s2, const float (&b)[24], int iters,
+                                                   float eps, float (&p)[4], float (&u)[4],
+                                                   float (&c)[16]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    p[j] = sigmoid_f(fmaf(m[j], s0, __ldg(base + j))) + eps;
-    u[j] = 2.0f * sigmoid_f(fmaf(m[4 + j], s1, __ldg(base + 4 + j)));
+    p[j] = sigmoid_f(fmaf(m[j], s0, b[j])) + eps;
+    u[j] = 2.0f * sigmoid_f(fmaf(m[4 + j], s1, b[4 + j]));
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float* row = c + 4 * j;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) row[k] = fmaf(m[8 + 4 * j + k], s2, __ldg(base + 8 + 4 * j + k));
+    for (int k = 0; k < 4; ++k) row[k] = fmaf(m[8 + 4 * j + k], s2, b[8 + 4 * j + k]);
     const float mx = fmaxf(fmaxf(row[0], row[1]), fmaxf(row[2], row[3]));
 #pragma unroll
     for (int k = 0; k < 4; ++k) row[k] = expf(row[k] - mx);
@@ -157,6 +157,16 @@ __device__ __forceinline__ void split_sinkhorn_all(const float (&m)[24], float s
     }
     col_step();
   }
+}
+// ... with the biases read from global memory.
+__device__ __forceinline__ void split_sinkhorn_all(const float (&m)[24], float s0, float s1,
+                                                   float s2, const float* __restrict__ base,
+                                                   int iters, float eps, float (&p)[4],
+                                                   float (&u)[4], float (&c)[16]) {
+  float b[24];
+#pragma unroll
+  for (int e = 0; e < 24; ++e) b[e] = __ldg(base + e);
+  split_sinkhorn_all(m, s0, s1, s2, b, iters, eps, p, u, c);
 }
 
 }  // namespace mhc

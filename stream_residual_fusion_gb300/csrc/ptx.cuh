@@ -358,6 +358,70 @@ __device__ __forceinline__ bool gwait(const unsigned* ctr, unsigned target, uint
 }
 
 // ---------------------------------------------------------------------------------------------
+// thread-block clusters: distributed shared memory
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of the cluster arrives once (release: its earlier writes, mbarrier initialisation
+// included, become visible to the cluster) and later waits once (acquire) before it touches
+// another CTA's shared memory.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// The shared::cluster address of shared-memory offset `saddr` in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// 16 bytes into another CTA's shared memory; the store counts its bytes as completed
+// transactions on that CTA's mbarrier `rbar` (both shared::cluster addresses of the same CTA).
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+      : "memory");
+}
+// mbarrier wait whose completion orders the cluster's writes that completed it (st.async) before
+// this thread's later reads; gives up after `limit_ns` like mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// block barriers
+
+// Barrier of every thread of the block, counted thread by thread (barrier.sync without .aligned).
+// __syncthreads is the aligned form, which requires every lane of a warp to reach it together:
+// in a kernel whose warps split their lanes between roles (one lane issuing copies while the
+// others wait), a warp may reach it in several parts, and the aligned barrier then completed before
+// every warp had arrived (measured: a CTA's thread 0 passed it 2 us before its finisher warp got
+// there). This form waits for all threads.
+__device__ __forceinline__ void block_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------------
 // named barriers (a subset of the block's warps)
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

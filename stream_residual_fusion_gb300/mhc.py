@@ -35,6 +35,8 @@ DEBUG_NEVER_ARRIVE = 0x2
 DEBUG_PLANT_OOB = 0x4          # bounds-checked build only
 SPLIT_SHIFT = 8
 TILE_SHIFT = 16
+PATH_PERSISTENT = 0x8          # the persistent (cooperative) kernel
+PATH_CLUSTER = 0x10            # the cluster kernel (one thread-block cluster per 40 tokens)
 
 N_STREAMS = 4
 MIX = (2 + N_STREAMS) * N_STREAMS
@@ -80,6 +82,7 @@ SIGNATURES = {
     "mhc_set_trace": (_I, [_P, _I64]),
     "mhc_step_config": (_I, [_I64, _I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(_I)]),
+    "mhc_step_path": (_I, [_I64, _I, _I, _U]),
     "mhc_version": (_I, []),
     "mhc_checked_build": (_I, []),
 }
@@ -445,6 +448,15 @@ def step_config(N: int, d: int, flags: int = 0, n: int = N_STREAMS):
     _check(lib.mhc_step_config(N, n, d, flags, ctypes.byref(sp), ctypes.byref(tt), ctypes.byref(gr)),
            "mhc_step_config")
     return sp.value, tt.value, gr.value
+
+
+def step_path(N: int, d: int, flags: int = 0, n: int = N_STREAMS) -> int:
+    """PATH_PERSISTENT or PATH_CLUSTER: the kernel the fused step runs for N tokens on the
+    current device."""
+    r = lib.mhc_step_path(N, n, d, flags)
+    if r < 0:
+        _check(r, "mhc_step_path")
+    return r
 
 
 def set_trace(buffer=None):

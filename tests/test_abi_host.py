@@ -265,3 +265,25 @@ def test_backward_validation(M):
     assert M.lib.mhc_backward_workspace_bytes(256, 4, 5120 + 32) == 0
     assert M.lib.mhc_backward_workspace_bytes(256, 3, 5120) == 0
 
+
+
+def test_path_flags_validation(M):
+    """MHC_PATH_PERSISTENT / MHC_PATH_CLUSTER: host-side checks, before any device call."""
+    P, C = M.PATH_PERSISTENT, M.PATH_CLUSTER
+    assert _fused(M, N=0, flags=P) == M.MHC_OK
+    assert _fused(M, N=0, flags=C) == M.MHC_OK                            # 16 CTAs of 320 columns
+    assert _fused(M, flags=P | C) == M.MHC_ERR_SHAPE
+    assert _fused(M, flags=C | M.tile_flag(32)) == M.MHC_ERR_SHAPE        # the tile is fixed at 32
+    assert _fused(M, flags=C | M.split_flag(32)) == M.MHC_ERR_SHAPE       # clusters of 8 or 16
+    assert _fused(M, flags=C | M.split_flag(8)) == M.MHC_ERR_SHAPE        # 20 chunks per CTA
+    assert _fused(M, N=0, d=2560, flags=C | M.split_flag(8)) == M.MHC_OK  # 10 chunks per CTA
+    assert _fused(M, N=0, d=256, flags=C) == M.MHC_OK                     # 8 CTAs of one chunk
+    assert _fused(M, d=6144, flags=C) == M.MHC_ERR_SHAPE                  # 12 or 24 chunks
+    assert _fused(M, N=0, d=6144, flags=P) == M.MHC_OK
+    p = [_addr(i) for i in range(16)]
+    assert M.lib.mhc_fused_step_mxfp8(*p, 0, 4, 5120, 20, 1e-6, 1e-6, C, _addr(21), 1 << 26,
+                                      None) == M.MHC_ERR_SHAPE             # bf16 y only
+    q = [_addr(i) for i in range(8)]
+    assert M.lib.mhc_mixes(*q, 0, 4, 5120, 20, 1e-6, 1e-6, C, _addr(9), 1 << 26,
+                           None) == M.MHC_ERR_SHAPE
+    assert M.lib.mhc_step_path(8, 4, 5120, P | C) == M.MHC_ERR_SHAPE

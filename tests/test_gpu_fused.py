@@ -197,23 +197,26 @@ def test_fused_tile_heights(M, synth, N, d, tile):
 
 
 def test_automatic_shape_choice(M):
-    """The automatic launch shape minimises the busiest group's rounds x slots x (height + fixed
-    slot cost) over the splits that fit and the heights that are multiples of the split: the
-    fewest CTAs per tile and 128-token tiles for the B=4, T=8192 batch, wider groups for decode."""
-    split, _, groups = M.step_config(32768, 5120)
+    """The persistent kernel's automatic launch shape minimises the busiest group's rounds x slots
+    x (height + fixed slot cost) over the splits that fit and the heights that are multiples of
+    the split: the fewest CTAs per tile and 128-token tiles for the B=4, T=8192 batch, wider
+    groups for decode (where the cluster kernel runs by default: test_gpu_cluster.py)."""
+    P = M.PATH_PERSISTENT
+    split, _, groups = M.step_config(32768, 5120, P)
     ctas = split * groups
 
     def cost(N, s, t):
         return -(-(-(-N // t)) // (ctas // s)) * (5120 // (32 * s)) * (t + 96)
     for N in (256, 4096, 32768, 131072, 1000):
-        split, tile, groups = M.step_config(N, 5120)
+        split, tile, groups = M.step_config(N, 5120, P)
         assert tile % 8 == 0 and 8 <= tile <= 128 and tile % split == 0
         options = [cost(N, s, t) for s in (8, 16, 32) for t in range(128, 7, -8) if t % s == 0]
         assert cost(N, split, tile) == min(options), N
+    assert M.step_config(32768, 5120) == M.step_config(32768, 5120, P)
     if ctas == 152:
-        assert M.step_config(32768, 5120)[:2] == (8, 128)
-        assert M.step_config(4096, 5120)[:2] == (8, 112)
-        assert M.step_config(256, 5120)[:2] == (32, 64)
+        assert M.step_config(32768, 5120, P)[:2] == (8, 128)
+        assert M.step_config(4096, 5120, P)[:2] == (8, 112)
+        assert M.step_config(256, 5120, P)[:2] == (32, 64)
 
 
 def test_fused_step_in_cuda_graph(M, synth):

@@ -30,10 +30,13 @@ def synth():
 
 
 def _both(M, inp, flags=0):
+    """The bf16-y step on the persistent kernel (the kernel the MXFP8 form runs) and the MXFP8
+    form."""
     Wp = M.pack_weights(inp["W"])
     args = (inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"])
     tail = (inp["scale"], inp["base"], inp["gain"])
-    bf = M.fused_step(*args, None, *tail, W_packed=Wp, flags=flags, with_mixes=True)
+    bf = M.fused_step(*args, None, *tail, W_packed=Wp, flags=flags | M.PATH_PERSISTENT,
+                      with_mixes=True)
     q = M.fused_step_mxfp8(*args, Wp, *tail, flags=flags, with_mixes=True)
     assert M.get_status() == M.MHC_OK
     return bf, q
@@ -83,7 +86,7 @@ def test_mxfp8_comb_row_dest_in_place_no_mixes(M, synth):
     Wp = M.pack_weights(inp["W"])
     tail = (inp["scale"], inp["base"], inp["gain"])
     bf = M.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None, *tail,
-                      W_packed=Wp, flags=M.COMB_ROW_DEST)
+                      W_packed=Wp, flags=M.COMB_ROW_DEST | M.PATH_PERSISTENT)
     X = inp["X"].clone()
     q = M.fused_step_mxfp8(X, inp["F"], inp["pre"], inp["post"], inp["comb"], Wp, *tail,
                            flags=M.COMB_ROW_DEST, out={"Xp": X})
@@ -128,7 +131,7 @@ def test_mxfp8_workload_full(M, synth):
     q = M.fused_step_mxfp8(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], Wp,
                            inp["scale"], inp["base"], inp["gain"])
     bf = M.fused_step(inp["X"], inp["F"], inp["pre"], inp["post"], inp["comb"], None,
-                      inp["scale"], inp["base"], inp["gain"], W_packed=Wp)
+                      inp["scale"], inp["base"], inp["gain"], W_packed=Wp, flags=M.PATH_PERSISTENT)
     assert M.get_status() == M.MHC_OK
     _same_as_cast(q, bf["y"])                           # every token
     del bf
