@@ -282,7 +282,8 @@ def run_table(args):
                 b.record()
             torch.cuda.synchronize()
             ms = sorted(a.elapsed_time(b) for a, b in ev[10:])
-            row.update(gpu_launches=reps, gpu_p50_ms=percentile(ms, 50), gpu_p95_ms=percentile(ms, 95),
+            row.update(path=("cluster" if mhc.step_path(w.N, w.d) == mhc.PATH_CLUSTER else "persistent"),
+                       gpu_launches=reps, gpu_p50_ms=percentile(ms, 50), gpu_p95_ms=percentile(ms, 95),
                        gpu_p99_ms=percentile(ms, 99),
                        gpu_tok_s=w.N / (percentile(ms, 50) / 1e3),
                        frac_measured=algorithmic_bytes(w.N, w.d) / (percentile(ms, 50) / 1e3) / 1e9 / peak,
