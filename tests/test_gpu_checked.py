@@ -145,3 +145,31 @@ def test_planted_out_of_range_rows_are_caught(M, MC, synth, mx, N, split, tile):
         assert bool((got["y_scale"][differ] == SENTINEL).all())
     else:
         assert torch.equal(got["y"], ref["y"])
+
+
+@pytest.mark.parametrize("N,d", [(100, 5120), (41, 1024)])
+def test_cluster_kernel_checked_build(M, MC, synth, N, d):
+    """The cluster kernel (MHC_PATH_CLUSTER) in the bounds-checked build: no check fires on a
+    regular call and the results equal the regular build's; the planted out-of-range row of the
+    first token's finisher store is caught and skipped, every other row written."""
+    inp = synth.make_inputs(N, 4, d, seed=970 + N, device=DEV, scale_uniform=True)
+    inp.pop("outliers", None)
+    Wp = M.pack_weights(inp["W"])
+    flags = MC.PATH_CLUSTER
+    full, view = _padded_outputs(N, d, False, 2 * N + 64)
+    got = _step(MC, inp, Wp, False, flags, view)
+    assert MC.get_status() == MC.MHC_OK
+    _padding_untouched(full, N)
+    ref = _step(M, inp, Wp, False, flags, None)
+    assert M.get_status() == M.MHC_OK
+    for k in view:
+        assert torch.equal(got[k], ref[k]), k
+    check_step(got, oracle_step(inp))
+    full, view = _padded_outputs(N, d, False, 2 * N + 64)
+    got = _step(MC, inp, Wp, False, flags | MC.DEBUG_PLANT_OOB, view)
+    assert MC.get_status() == MC.MHC_ERR_BOUNDS
+    _padding_untouched(full, N)
+    for k in ("pre", "post", "comb", "mixes"):
+        assert bool((got[k][0].view(torch.uint8) == SENTINEL).all()), k
+        assert torch.equal(got[k][1:], ref[k][1:]), k
+    assert torch.equal(got["Xp"], ref["Xp"]) and torch.equal(got["y"], ref["y"])
