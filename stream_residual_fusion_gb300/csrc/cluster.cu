@@ -16,8 +16,8 @@
 //     contiguous run of 32 CL columns of each token row. 40-token tiles: a GB300 runs 7 clusters
 //     of 16 CTAs at once (a cluster's CTAs share a GPC), so 256 tokens take one wave.
 //   * Every chunk of X and F stays in shared memory for the whole kernel (S x 15 KB): no ring to
-//     recycle. The bulk copies one thread issues are served one after another (about 0.5 us each,
-//     measured, small or large), so every tile has a lane of its own: lane L of warp 0 copies
+//     recycle. The bulk copies one thread issues are served one after another (about 0.35 us each
+//     in a probe, 8 KB or 16 KB), so every tile has a lane of its own: lane L of warp 0 copies
 //     tiles L and L + 32 of the 5 S (X_0..X_3 and F of each chunk) and later stores X' or y from
 //     them. Warp 0 also refills the weight ring, so that the MMA lane never waits for its own MMAs
 //     to complete (a lane spinning on that wait, diverged from the MMA lane in the same warp,

@@ -16,41 +16,61 @@ namespace {
 // kernel's shared-memory image: column block jb (STEP_WDC columns of every stream) is
 // [4 streams][80 rows][STEP_WDC columns] with plane pl of mix row r in row packed_row(r, pl),
 // rows 72..79 zero, and the 16-byte chunks of each row swizzled as the tensor cores read them.
-// One thread per 16-byte output chunk.
+// One thread per 8 weights (a 16-byte chunk of each plane): it reads them once and writes all
+// three planes; the threads past those write the zero rows.
 __global__ void pack_kernel(const float* __restrict__ W, uint8_t* __restrict__ P, int d) {
   const int64_t K = 4 * static_cast<int64_t>(d);
   const int64_t nblocks = d / STEP_WDC;
-  const int64_t total = nblocks * 4 * STEP_MMA_N * STEP_WCHUNKS;
+  constexpr int MIXR = STEP_WROWS / 3;                          // 24 mix rows
+  constexpr int PADR = STEP_MMA_N - STEP_WROWS;                 // 8 zero rows
+  const int64_t main_items = nblocks * 4 * MIXR * STEP_WCHUNKS;
+  const int64_t total = main_items + nblocks * 4 * PADR * STEP_WCHUNKS;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int chunk = static_cast<int>(idx % STEP_WCHUNKS);
-    const int row = static_cast<int>((idx / STEP_WCHUNKS) % STEP_MMA_N);
-    const int k = static_cast<int>((idx / (STEP_WCHUNKS * STEP_MMA_N)) % 4);
-    const int64_t jb = idx / (STEP_WCHUNKS * STEP_MMA_N * 4);
-    uint32_t words[4] = {0u, 0u, 0u, 0u};
-    if (row < STEP_WROWS) {
-      const int half = row / 36, rem = row % 36;
-      const int pl = rem / 12;
-      const int r = 12 * half + rem % 12;
+    if (idx < main_items) {
+      // consecutive threads: the chunks of one row, then the rows (mix numbers), so a warp reads
+      // 8 rows x 128 contiguous bytes of W
+      const int chunk = static_cast<int>(idx % STEP_WCHUNKS);
+      const int r = static_cast<int>((idx / STEP_WCHUNKS) % MIXR);
+      const int k = static_cast<int>((idx / (STEP_WCHUNKS * MIXR)) % 4);
+      const int64_t jb = idx / (STEP_WCHUNKS * MIXR * 4);
       const int64_t col = k * static_cast<int64_t>(d) + jb * STEP_WDC + chunk * 8;
-      __nv_bfloat16 v[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float w = W[r * K + col + e];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-        const float rem1 = w - __bfloat162float(hi);
-        const __nv_bfloat16 mid = __float2bfloat16_rn(rem1);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(rem1 - __bfloat162float(mid));
-        v[e] = pl == 0 ? hi : (pl == 1 ? mid : lo);
-      }
+      const float4* src = reinterpret_cast<const float4*>(W + r * K + col);
+      const float4 a = src[0], b = src[1];
+      const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t planes[3][4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        words[e] = static_cast<uint32_t>(__bfloat16_as_ushort(v[2 * e])) |
-                   (static_cast<uint32_t>(__bfloat16_as_ushort(v[2 * e + 1])) << 16);
+        uint32_t hv[2], mv[2], lv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float x = w[2 * e + h];
+          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+          const float rem1 = x - __bfloat162float(hi);
+          const __nv_bfloat16 mid = __float2bfloat16_rn(rem1);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(rem1 - __bfloat162float(mid));
+          hv[h] = __bfloat16_as_ushort(hi);
+          mv[h] = __bfloat16_as_ushort(mid);
+          lv[h] = __bfloat16_as_ushort(lo);
+        }
+        planes[0][e] = hv[0] | (hv[1] << 16);
+        planes[1][e] = mv[0] | (mv[1] << 16);
+        planes[2][e] = lv[0] | (lv[1] << 16);
       }
+      uint8_t* blk = P + jb * STEP_WBLOCK_BYTES + k * STEP_WSTREAM_BYTES;
+#pragma unroll
+      for (int pl = 0; pl < 3; ++pl)
+        *reinterpret_cast<uint4*>(blk + wtile_chunk_offset(packed_row(r, pl), chunk)) =
+            make_uint4(planes[pl][0], planes[pl][1], planes[pl][2], planes[pl][3]);
+    } else {
+      const int64_t q = idx - main_items;
+      const int chunk = static_cast<int>(q % STEP_WCHUNKS);
+      const int row = STEP_WROWS + static_cast<int>((q / STEP_WCHUNKS) % PADR);
+      const int k = static_cast<int>((q / (STEP_WCHUNKS * PADR)) % 4);
+      const int64_t jb = q / (STEP_WCHUNKS * PADR * 4);
+      *reinterpret_cast<uint4*>(P + jb * STEP_WBLOCK_BYTES + k * STEP_WSTREAM_BYTES +
+                                wtile_chunk_offset(row, chunk)) = make_uint4(0u, 0u, 0u, 0u);
     }
-    uint8_t* dst = P + jb * STEP_WBLOCK_BYTES + k * STEP_WSTREAM_BYTES + wtile_chunk_offset(row, chunk);
-    *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
   }
 }
 
@@ -264,7 +284,9 @@ int grid_for(int64_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_pack(const float* W, void* packed, int d, cudaStream_t stream) {
-  const int64_t chunks = static_cast<int64_t>(d / STEP_WDC) * 4 * STEP_MMA_N * STEP_WCHUNKS;
+  // one thread per 8 weights of a mix row, plus one per 16-byte chunk of the zero rows
+  const int64_t chunks = static_cast<int64_t>(d / STEP_WDC) * 4 *
+                         (STEP_WROWS / 3 + STEP_MMA_N - STEP_WROWS) * STEP_WCHUNKS;
   pack_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(W, static_cast<uint8_t*>(packed), d);
   return cudaGetLastError();
 }
