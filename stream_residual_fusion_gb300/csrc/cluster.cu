@@ -559,14 +559,20 @@ bool cmap_rows(CUtensorMap* m, const void* p, int64_t N, int d) {   // [N, d]
   return cmap(m, p, 2, dims, str, box);
 }
 
+// The kernel's attributes on the current device (they are per device: set once for each).
 cudaError_t prepare() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(cluster_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CSMEM);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(cluster_step_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  });
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  err = cudaFuncSetAttribute(cluster_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CSMEM);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(cluster_step_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (err == cudaSuccess) done[dev] = true;
   return err;
 }
 

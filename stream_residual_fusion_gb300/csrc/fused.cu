@@ -41,6 +41,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -1267,22 +1268,26 @@ bool map_rows(CUtensorMap* m, const void* p, int64_t rows, int64_t cols, uint32_
 }
 
 
-// CTAs of the step kernel the current device holds at once (one per SM).
+// CTAs of the step kernel the current device holds at once (one per SM), cached per device.
 template <typename Kern>
 cudaError_t resident_ctas(Kern kern, int* ctas) {
-  static int cache[3] = {0, 0, 0};
+  constexpr int kDevices = 64;
+  static std::atomic<int> cache[3][kDevices] = {};
   const int which = (kern == step_kernel<true>) ? 1 : (kern == step_kernel<true, true>) ? 2 : 0;
-  if (cache[which] > 0) {
-    *ctas = cache[which];
-    return cudaSuccess;
-  }
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+  const int cached = cache[which][dev].load(std::memory_order_relaxed);
+  if (cached > 0) {
+    *ctas = cached;
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NTHREADS, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  cache[which] = sms * per_sm;
-  *ctas = cache[which];
+  cache[which][dev].store(sms * per_sm, std::memory_order_relaxed);
+  *ctas = sms * per_sm;
   return cudaSuccess;
 }
 
