@@ -777,18 +777,19 @@ __global__ void pack_wt_kernel(const float* __restrict__ W, uint8_t* __restrict_
 // The contraction runs over tokens, so both operands are read token-major as TMA lays them
 // down: A = X'^T (M = 128 of the block's 256 (stream, column) values, MN-major, 128-byte
 // swizzle: 64 columns of one stream per 128-byte row, two streams LBO apart, 8-token groups
-// 1 KB apart) and B = the bf16 planes of r g_m (N = 32 mix rows of which 24 are used, MN-major,
-// 64-byte swizzle). hi and lo planes accumulate into the same fp32 accumulator (X' is exact in
-// bf16). Two accumulators of [128 x 32] (streams 0-1 and 2-3) stay in TMEM for the whole range.
+// 1 KB apart) and B = both bf16 planes of r g_m side by side (N = 64: hi in columns 0-31, lo in
+// 32-63, 24 mix rows of each used; MN-major, 128-byte swizzle), so one MMA takes a K-step of
+// both planes: 8 MMAs per stage. Two accumulators of [128 x 64] (streams 0-1 and 2-3, hi then lo
+// columns) stay in TMEM for the whole range; the epilogue adds each row's hi and lo sums (X' is
+// exact in bf16).
 
 constexpr int WT_COLS = 64;                  // columns per work item (of each stream)
 constexpr int WT_TB = 64;                    // tokens per stage (four MMA K-steps)
 constexpr int WT_NST = 4;                    // stages
 constexpr int WT_XB = WT_TB * 128;           // one X'_k box: [64 tokens x 64 columns] bf16
 constexpr int WT_OFF_GY = 4 * WT_XB;
-constexpr int WT_OFF_GH = WT_OFF_GY + WT_XB;         // [64 tokens x 32] bf16, 64-byte rows
-constexpr int WT_OFF_GL = WT_OFF_GH + WT_TB * 64;
-constexpr int WT_OFF_P = WT_OFF_GL + WT_TB * 64;     // p_prev [64][4] fp32
+constexpr int WT_OFF_G = WT_OFF_GY + WT_XB;          // planes [64 tokens x (32 hi | 32 lo)] bf16
+constexpr int WT_OFF_P = WT_OFF_G + WT_TB * 128;     // p_prev [64][4] fp32
 constexpr int WT_OFF_R = WT_OFF_P + WT_TB * 16;      // {r, r_y, tau, c1} [64][4] fp32
 constexpr int WT_STAGE = WT_OFF_R + WT_TB * 16;
 constexpr int WT_OFF_RED = WT_NST * WT_STAGE;        // ggain partials [4 phases][64 columns]
@@ -801,7 +802,7 @@ static_assert(WT_STAGE % 1024 == 0, "stage alignment (128-byte swizzle)");
 static_assert(WT_SMEM <= 232448, "shared memory budget");
 constexpr int WT_CONS = 4;                   // consumer / epilogue warps (2..5)
 constexpr int WT_THREADS = (2 + WT_CONS) * 32;
-constexpr uint32_t WT_TMEM_COLS = 64;
+constexpr uint32_t WT_TMEM_COLS = 128;
 
 // Shared-memory descriptor of an MN-major operand: `row_bytes` (64 or 128) of the MN dimension
 // per row with the swizzle of that width, consecutive K rows row_bytes apart, 8-row K groups
@@ -884,13 +885,12 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
           const uint32_t nt = static_cast<uint32_t>(std::min<int64_t>(WT_TB, P.N - tb));
           uint8_t* st = sm + b * WT_STAGE;
           // the boxes always move WT_TB rows (rows past N read as zero); p and rec move nt rows
-          mbar_arrive_expect_tx(&full[b], 5u * WT_XB + 2u * WT_TB * 64 + 2u * nt * 16);
+          mbar_arrive_expect_tx(&full[b], 5u * WT_XB + WT_TB * 128u + 2u * nt * 16);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             tma_load_3d_hint(st + k * WT_XB, &tm_xp, &full[b], cb * WT_COLS, k, static_cast<int>(tb), pol);
           tma_load_2d_hint(st + WT_OFF_GY, &tm_gy, &full[b], cb * WT_COLS, static_cast<int>(tb), pol);
-          tma_load_2d(st + WT_OFF_GH, &tm_gp, &full[b], 0, static_cast<int>(tb));
-          tma_load_2d(st + WT_OFF_GL, &tm_gp, &full[b], 32, static_cast<int>(tb));
+          tma_load_2d(st + WT_OFF_G, &tm_gp, &full[b], 0, static_cast<int>(tb));
           bulk_load_hint(st + WT_OFF_P, P.pre_prev + tb * 4, nt * 16, &full[b], pol);
           bulk_load_hint(st + WT_OFF_R, P.rec + tb * 4, nt * 16, &full[b], pol);
         }
@@ -899,8 +899,8 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // bf16 A and B, fp32 D, M = 128, N = 32, both operands MN-major
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 32) | (1u << 15) | (1u << 16);
+      // bf16 A and B, fp32 D, M = 128, N = 64 (both planes), both operands MN-major
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 64) | (1u << 15) | (1u << 16);
       int g = 0, it = 0;
       for (int64_t item = blockIdx.x; item < items; item += gridDim.x, ++it) {
         int64_t t0, t1;
@@ -917,14 +917,10 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-            for (int pl = 0; pl < 2; ++pl) {
-#pragma unroll
-              for (int ks = 0; ks < WT_TB / 16; ++ks) {
-                const uint64_t a = sdesc_mnmajor(st + 2 * mt * WT_XB + ks * 2048, 128, WT_XB, 1024);
-                const uint64_t bd = sdesc_mnmajor(st + (pl ? WT_OFF_GL : WT_OFF_GH) + ks * 1024, 64, 0, 512);
-                umma_bf16(tmem + static_cast<uint32_t>(mt * 32), a, bd, idesc,
-                          (first && pl == 0 && ks == 0) ? 0u : 1u);
-              }
+            for (int ks = 0; ks < WT_TB / 16; ++ks) {
+              const uint64_t a = sdesc_mnmajor(st + 2 * mt * WT_XB + ks * 2048, 128, WT_XB, 1024);
+              const uint64_t bd = sdesc_mnmajor(st + WT_OFF_G + ks * 2048, 128, 0, 1024);
+              umma_bf16(tmem + static_cast<uint32_t>(mt * 64), a, bd, idesc, (first && ks == 0) ? 0u : 1u);
             }
           }
           first = false;
@@ -973,22 +969,24 @@ __global__ void __launch_bounds__(WT_THREADS, 1)
         if (lane == 0) mbar_arrive(&empty[b]);
       }
       // gW partials of the range: accumulator mt holds (stream 2mt + m / 64, column m % 64) in
-      // TMEM lane m, mix row o in column 32 mt + o
+      // TMEM lane m, mix row o's hi-plane sum in column 64 mt + o and lo-plane sum in 64 mt + 32 + o
       if (!mbar_wait(dfull, it & 1, limit())) timed_out = true;
       tc_fence_after();
       float* pw = P.partW + static_cast<int64_t>(tr) * MIXN * 4 * P.d;
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 32), v);
+        uint32_t v[32], w[32];
+        tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 64), v);
+        tmem_ld_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 64 + 32), w);
         if (t1 <= t0) {   // a range past the last token: no MMA ran, its sums are zero
 #pragma unroll
-          for (int o = 0; o < 32; ++o) v[o] = 0u;
+          for (int o = 0; o < 32; ++o) v[o] = w[o] = 0u;
         }
         const int m = q * 32 + lane;
         const int64_t col = static_cast<int64_t>(2 * mt + (m >> 6)) * P.d + cb * WT_COLS + (m & 63);
 #pragma unroll
-        for (int o = 0; o < MIXN; ++o) pw[static_cast<int64_t>(o) * 4 * P.d + col] = __uint_as_float(v[o]);
+        for (int o = 0; o < MIXN; ++o)
+          pw[static_cast<int64_t>(o) * 4 * P.d + col] = __uint_as_float(v[o]) + __uint_as_float(w[o]);
       }
       tc_fence_before();
       __syncwarp();
@@ -1212,7 +1210,7 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t stream) {
     CUtensorMap txp, tgy, tgp;
     if (!bmap_streams_box(&txp, a.Xp, N, d, WT_COLS, WT_TB, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !bmap_rows(&tgy, a.gy, N, d, WT_COLS, WT_TB, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !bmap_rows(&tgp, ws + L.off_gpl, N, 64, 32, WT_TB, CU_TENSOR_MAP_SWIZZLE_64B))
+        !bmap_rows(&tgp, ws + L.off_gpl, N, 64, 64, WT_TB, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     WtParams W{};
     W.partW = wsf(L.off_partW);
