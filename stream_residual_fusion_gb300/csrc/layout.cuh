@@ -8,9 +8,9 @@
 namespace mhc {
 
 // A pipeline slot is STEP_TT token rows of STEP_DC columns of X_0..X_3 and F: 40 KB, so four
-// slots fit in shared memory. (The kernel also builds with 64 x 64 slots, whose 128-byte rows
-// DRAM serves better; measured slower at d = 5120: every weight block then serves half as many
-// tokens, and each group walks twice the tiles.)
+// slots fit in shared memory. (Slots of 64 tokens x 64 columns, the same 40 KB with 128-byte
+// rows that DRAM serves better, measured slower at d = 5120: each slot then takes 16 MMAs and a
+// fold, every weight block serves half as many tokens, and each group walks twice the tiles.)
 constexpr int STEP_TT = 128;     // token rows per tile (the MMA's M)
 constexpr int STEP_DC = 32;
 constexpr int STEP_ROW_BYTES = STEP_DC * 2;
@@ -34,7 +34,7 @@ __host__ __device__ constexpr uint32_t swizzled_chunk_offset(int row, int chunk,
   return static_cast<uint32_t>(row * row_bytes +
                                ((chunk ^ ((row * row_bytes >> 7) & (row_bytes / 16 - 1))) << 4));
 }
-// ... of an X/F tile (128-byte rows) and of a packed weight tile (64-byte rows)
+// ... of an X/F tile (STEP_ROW_BYTES-byte rows) and of a packed weight tile (64-byte rows)
 __host__ __device__ constexpr uint32_t tile_chunk_offset(int row, int chunk) {
   return swizzled_chunk_offset(row, chunk, STEP_ROW_BYTES);
 }
