@@ -268,7 +268,7 @@ def run_table(args):
                                  inp["scale"], inp["base"], inp["gain"], W_packed=Wp,
                                  scratch=scratch)
             flush = (torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-                     if w.N * STREAM_BYTES_PER_TOKEN < 2 * L2_BYTES else None)
+                     if fits_in_l2(w.N) else None)
             reps = 20 if w.N >= 100000 else 100
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(reps + 10)]
@@ -295,6 +295,12 @@ def run_table(args):
     return 0
 
 
+def fits_in_l2(n_tokens: int) -> bool:
+    """A step's streams (read and written) fit in twice L2: such workloads flush L2 before every
+    timed launch, larger ones are timed back to back."""
+    return n_tokens * STREAM_BYTES_PER_TOKEN < 2 * L2_BYTES
+
+
 def workload_config(w, n_total: int, n_rank: int) -> dict:
     """The workload both arms report (the reference arm's oracle runs a bounded sample of it,
     described in its cpu_baseline.sample)."""
@@ -302,7 +308,7 @@ def workload_config(w, n_total: int, n_rank: int) -> dict:
             "d": w.d, "tokens_per_rank": n_rank, "sinkhorn_iters": 20,
             "comb_reading": "code: X'_k = u_k F + sum_j C_jk X_j",
             "l2": (f"inputs larger than L2 ({n_rank * 51200 / 1e9:.2f} GB of streams read per step)"
-                   if n_rank * STREAM_BYTES_PER_TOKEN >= 2 * L2_BYTES else
+                   if not fits_in_l2(n_rank) else
                    "inputs smaller than L2: a 256 MB write flushes L2 before every timed step, "
                    "outside the step's own events, whose mean is ms_per_step")}
 
@@ -431,7 +437,7 @@ def run_ours(args):
     # Workloads whose streams fit in L2: a 256 MB write flushes it before every timed step,
     # outside events that bracket the whole step, and the step time is the mean of those.
     flush = (torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-             if N * STREAM_BYTES_PER_TOKEN < 2 * L2_BYTES else None)
+             if fits_in_l2(N) else None)
     st = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         dist.barrier()

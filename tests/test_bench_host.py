@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py (no GPU): the algorithmic byte counts it reports, checked against
-the oracle's pinned traffic counts, and the lookup of the committed ncu traffic summary."""
+the oracle's pinned traffic counts, the lookup of the committed ncu traffic summary, and which
+workloads are timed with L2 flushed."""
 import pytest
 
 import bench
@@ -43,3 +44,16 @@ def test_percentile_interpolates_between_ranks():
     assert bench.percentile(xs, 99) == pytest.approx(198.01)
     assert bench.percentile(xs, 0) == 1.0 and bench.percentile(xs, 100) == 200.0
     assert bench.percentile([3.0], 95) == 3.0 and bench.percentile([], 50) is None
+
+
+def test_small_workloads_are_timed_with_l2_flushed():
+    """The two batches whose streams fit in L2 (8 and 256 tokens) flush it before every timed
+    step and say so in config.l2; the prefill batches are larger than L2 and say that."""
+    from stream_residual_fusion_gb300 import synth
+    flushed = {name: bench.fits_in_l2(w.N) for name, w in synth.WORKLOADS.items()}
+    assert flushed == {"tiny": True, "decode256": True, "prefill4k": False, "prefill32k": False,
+                       "prefill128k": False}
+    for name, w in synth.WORKLOADS.items():
+        l2 = bench.workload_config(w, w.N, w.N)["l2"]
+        assert l2.startswith("inputs smaller than L2: a 256 MB write flushes L2") == flushed[name], name
+        assert l2.startswith("inputs larger than L2") == (not flushed[name]), name
