@@ -544,7 +544,8 @@ def run_ours(args):
     fused_avg = statistics.mean(fused_ms)
     achieved = algorithmic_bytes(N, d) / (fused_avg / 1e3) / 1e9
     peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
-    traffic = ncu_traffic(N)
+    # the committed DRAM counts are the persistent kernel's: none for the cluster kernel's line
+    traffic = ncu_traffic(N) if path == "persistent" else None
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
