@@ -344,13 +344,15 @@ int mhc_step_path(int64_t N, int n, int d, unsigned flags);
  * is `split` CTAs, one per SM). On the cluster path (mhc_step_path): the cluster size, 40, and
  * the number of clusters. Diagnostic; needs a GPU.                                           */
 int mhc_step_config(int64_t N, int n, int d, unsigned flags, int* split, int* tile, int* groups);
-/* Phase tracing of the fused step (off by default). With a device buffer set, every later
- * launch whose grid fits records, per CTA, 8 uint64 values from the GPU's nanosecond timer:
- * the start time, then nanoseconds since the start at: loads issued, main loop done, partials
- * ready, cluster reduced, mix numbers written, y written, end (slot 7 carries the SM id in bits
- * 40 and up). CTA index = tile * split + rank in the cluster. Launches
- * with more CTAs than the buffer holds record nothing. NULL turns tracing off. The buffer stays
- * caller-owned; it must outlive the launches that write it. Not thread-safe.                  */
+/* Phase tracing of the fused step's persistent kernel (off by default; the cluster kernel
+ * records nothing). With a device buffer set, every later launch whose grid fits records, per
+ * (tile, rank in its group), 8 uint64 values from the GPU's nanosecond timer: slot 0 the tile's
+ * start; slots 1..6 nanoseconds since then at: the producer issued the tile's loads, the
+ * consumers' main loop done, the tile's partial sums posted, (unused), the finisher done, the
+ * consumers' tile end; slot 7 the nanoseconds to the kernel's end, with the SM id in bits 40
+ * and up. Record index = tile * split + rank. Launches with more records than the buffer holds
+ * (64 bytes each) record nothing. NULL turns tracing off. The buffer stays caller-owned; it
+ * must outlive the launches that write it. Not thread-safe.                                  */
 int mhc_set_trace(void* buffer, int64_t bytes);
 /* Static text for a status code.                                                              */
 const char* mhc_strerror(int code);
